@@ -1,0 +1,248 @@
+"""Python binding of libigc.so, the GB300 (sm_103a) tensor-core GEMM and
+implicit-GEMM convolution library.
+
+The functions here have the names of the C ABI (include/igc.h) and do
+argument marshalling only: they take torch tensors (device memory) and the
+current torch CUDA stream, pass raw pointers, sizes and strides to the C
+entry points, and raise IGCError on a non-zero status.  All computation runs
+in the library's CUDA kernels; there is no CPU fallback.  If the library is
+missing and cannot be built, importing the binding's functions raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+HEADER = os.path.join(_ROOT, "include", "igc.h")
+
+IGC_OK = 0
+IGC_ERR_INVALID_ARG = 1
+IGC_ERR_MISALIGNED = 2
+IGC_ERR_UNSUPPORTED = 3
+IGC_ERR_CUDA = 4
+IGC_ERR_DEVICE_TIMEOUT = 5
+IGC_ERR_WORKSPACE = 6
+IGC_F32 = 0
+IGC_F16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class IGCError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    from . import build as _b
+    return _b.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libigc.so (built in-tree on first use if out of date)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            from . import build as _b
+            path = _b.build()
+            if not os.path.exists(path):
+                raise ImportError(f"libigc.so missing at {path}")
+            L = ctypes.CDLL(path)
+            i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+            L.gemm_f16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp]
+            L.gemm_f16.restype = i32
+            L.gemm_s8_zp.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64,
+                                     ctypes.c_int32, vp, ctypes.c_int32, vp,
+                                     vp, i64, vp, i64, ctypes.c_float, vp, vp, sz, vp]
+            L.gemm_s8_zp.restype = i32
+            L.gemm_s8_zp_workspace_size.argtypes = [i64, i64, i64]
+            L.gemm_s8_zp_workspace_size.restype = sz
+            L.conv2d_nhwc_f16_implicit.argtypes = [i32] * 11 + [vp, vp, vp, vp, vp]
+            L.conv2d_nhwc_f16_implicit.restype = i32
+            L.igc_status_string.argtypes = [i32]
+            L.igc_status_string.restype = ctypes.c_char_p
+            L.igc_check_device_status.argtypes = [vp]
+            L.igc_check_device_status.restype = i32
+            L.igc_last_device_status.argtypes = []
+            L.igc_last_device_status.restype = ctypes.c_uint64
+            L.igc_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.igc_set_wait_limit_ns.restype = ctypes.c_uint64
+            L.igc_debug_wait_timeout_probe.argtypes = [vp]
+            L.igc_debug_wait_timeout_probe.restype = i32
+            L.igc_version.argtypes = []
+            L.igc_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/igc.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) -
+                  {"sizeof", "defined", "if"})
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc: int, what: str):
+    if rc != IGC_OK:
+        raise IGCError(rc, what)
+
+
+def _rows(t, name, dtype=None):
+    """(rows, cols, row stride in elements) of a 2-D row-major view."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major view with unit inner stride")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.shape[0], t.shape[1], max(t.stride(0), t.shape[1])
+
+
+def status_string(status: int) -> str:
+    return lib().igc_status_string(int(status)).decode()
+
+
+def igc_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def igc_check_device_status(stream=None) -> int:
+    return int(lib().igc_check_device_status(_stream(stream)))
+
+
+def igc_last_device_status() -> int:
+    return int(lib().igc_last_device_status())
+
+
+def igc_set_wait_limit_ns(limit_ns: int) -> int:
+    return int(lib().igc_set_wait_limit_ns(int(limit_ns)))
+
+
+def igc_debug_wait_timeout_probe(stream=None) -> int:
+    return int(lib().igc_debug_wait_timeout_probe(_stream(stream)))
+
+
+def igc_version() -> str:
+    return lib().igc_version().decode()
+
+
+# ---------------------------------------------------------------------------
+# the three operations
+# ---------------------------------------------------------------------------
+
+def gemm_f16(A, Bt, C=None, C_f32_check=None, stream=None):
+    """C[i,j] = sum_k A[i,k] Bt[j,k]; A (M,K) fp16, Bt (N,K) fp16 (B column-major),
+    C (M,N) fp16 or fp32, C_f32_check optional fp32 (M,N).  Returns C."""
+    import torch
+    M, K, lda = _rows(A, "A", torch.float16)
+    N, K2, ldb = _rows(Bt, "Bt", torch.float16)
+    if K2 != K:
+        raise ValueError("A and Bt disagree on K")
+    if C is None and C_f32_check is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    c_dtype, ldc = IGC_F32, 0
+    if C is not None:
+        m, n, ldc = _rows(C, "C", (torch.float16, torch.float32))
+        if (m, n) != (M, N):
+            raise ValueError("C has the wrong shape")
+        c_dtype = IGC_F16 if C.dtype == torch.float16 else IGC_F32
+    ldc32 = 0
+    if C_f32_check is not None:
+        m, n, ldc32 = _rows(C_f32_check, "C_f32_check", torch.float32)
+        if (m, n) != (M, N):
+            raise ValueError("C_f32_check has the wrong shape")
+    rc = lib().gemm_f16(M, N, K, _ptr(A), lda, _ptr(Bt), ldb, _ptr(C), ldc, c_dtype,
+                        _ptr(C_f32_check), ldc32, _stream(stream))
+    _check(rc, "gemm_f16")
+    return C
+
+
+def gemm_s8_zp_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().gemm_s8_zp_workspace_size(M, N, K))
+
+
+def gemm_s8_zp(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, C32=None, C8=None,
+               scale=0.0, scale_col=None, workspace=None, stream=None):
+    """INT8 GEMM with zero points: A (M,K) uint8/int8, Bt (N,K) uint8/int8.
+    Outputs C32 (M,N) int32 and/or C8 (M,N) int8.  Returns (C32, C8)."""
+    import torch
+    M, K, lda = _rows(A, "A", (torch.uint8, torch.int8))
+    N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8))
+    if K2 != K:
+        raise ValueError("A and Bt disagree on K")
+    ldc32 = ldc8 = 0
+    if C32 is not None:
+        m, n, ldc32 = _rows(C32, "C32", torch.int32)
+        if (m, n) != (M, N):
+            raise ValueError("C32 has the wrong shape")
+    if C8 is not None:
+        m, n, ldc8 = _rows(C8, "C8", torch.int8)
+        if (m, n) != (M, N):
+            raise ValueError("C8 has the wrong shape")
+    for v, name, n_, dt in ((zA_row, "zA_row", M, torch.int32), (zB_col, "zB_col", N, torch.int32),
+                            (scale_col, "scale_col", N, torch.float32)):
+        if v is not None and (v.dtype != dt or v.numel() != n_ or not v.is_contiguous() or not v.is_cuda):
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} vector of length {n_}")
+    need = gemm_s8_zp_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
+    rc = lib().gemm_s8_zp(M, N, K, _ptr(A), 1 if A.dtype == torch.int8 else 0, lda,
+                          _ptr(Bt), 1 if Bt.dtype == torch.int8 else 0, ldb,
+                          int(zA), _ptr(zA_row), int(zB), _ptr(zB_col),
+                          _ptr(C32), ldc32, _ptr(C8), ldc8, float(scale), _ptr(scale_col),
+                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _stream(stream))
+    _check(rc, "gemm_s8_zp")
+    return C32, C8
+
+
+def conv2d_nhwc_f16_implicit(x, w, y=None, y_f32_check=None, pad=(1, 1), stride=(1, 1),
+                             stream=None):
+    """y[n,p,q,k] = sum_{r,s,c} xpad[n, p*sh+r-ph, q*sw+s-pw, c] * w[k,r,s,c];
+    x NHWC fp16, w KRSC fp16, y NPQK fp16.  Returns y (or y_f32_check if y is None)."""
+    import torch
+    if x.dim() != 4 or w.dim() != 4 or x.dtype != torch.float16 or w.dtype != torch.float16:
+        raise ValueError("x and w must be 4-D fp16 tensors")
+    if not (x.is_contiguous() and w.is_contiguous() and x.is_cuda and w.is_cuda):
+        raise ValueError("x and w must be dense CUDA tensors")
+    N, H, W, C = x.shape
+    K, R, S, C2 = w.shape
+    if C2 != C:
+        raise ValueError("x and w disagree on C")
+    ph, pw = pad
+    sh, sw = stride
+    P = (H + 2 * ph - R) // sh + 1
+    Q = (W + 2 * pw - S) // sw + 1
+    if y is None and y_f32_check is None:
+        y = torch.empty((N, P, Q, K), dtype=torch.float16, device=x.device)
+    for t, dt, name in ((y, torch.float16, "y"), (y_f32_check, torch.float32, "y_f32_check")):
+        if t is not None and (tuple(t.shape) != (N, P, Q, K) or t.dtype != dt or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a dense ({N},{P},{Q},{K}) {dt} tensor")
+    rc = lib().conv2d_nhwc_f16_implicit(N, H, W, C, K, R, S, ph, pw, sh, sw, _ptr(x), _ptr(w),
+                                        _ptr(y), _ptr(y_f32_check), _stream(stream))
+    _check(rc, "conv2d_nhwc_f16_implicit")
+    return y if y is not None else y_f32_check

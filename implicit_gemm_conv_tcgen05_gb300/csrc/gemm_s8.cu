@@ -1,0 +1,185 @@
+// gemm_s8_zp: INT8 GEMM with input zero points and requantisation (page
+// "TVM在CUDA GPU上跑GEMM的全套张量化实现", §2.3: C = (A_q - zp_A)(B_q - zp_B)
+// accumulated in int32, dequantise / requantise fused into the GEMM).
+//
+// sm_103a has no integer tcgen05 MMA kind, so the contraction runs exactly on
+// the fp16 tensor pipe:
+//  1. pre-pass (HBM-bound, one read of A_q and B_q): A' = A_q - oA and
+//     B' = B_q - oB with oX = 128 for uint8, 0 for int8, so every value lies in
+//     [-128, 127] and is exact in fp16; written as fp16 into the workspace
+//     together with the sums rA'[i] = sum_k A'[i,k] and cB'[j] = sum_k B'[j,k].
+//  2. tcgen05 kind::f16 GEMM over A', B' in chunks of 256 k: each chunk's
+//     partial sums are integers of magnitude <= 256 * 128 * 128 = 2^22, so the
+//     fp32 accumulator holds them exactly; the epilogue drains every chunk into
+//     an int32 running sum S'[i,j] = sum_k A'[i,k] B'[j,k].
+//  3. fused epilogue, in int32 two's complement (mod 2^32):
+//        C32 = S' - zB'_j rA'_i - zA'_i cB'_j + K zA'_i zB'_j,
+//     with zA'_i = zA_i - oA and zB'_j = zB_j - oB -- the zero-point expansion of
+//     sum_k (A'[i,k] - zA'_i)(B'[j,k] - zB'_j) = sum_k (A_q - zA_i)(B_q - zB_j),
+//     then C8 = clamp(rne(fp32(C32) * scale_j), -128, 127).
+#include "launch.cuh"
+
+using namespace igc;
+
+namespace {
+
+constexpr size_t kWsAlign = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline long long k_padded(long long K) { return (K + 7) / 8 * 8; }  // 16-byte fp16 rows
+
+struct WsLayout {
+  size_t a_off, b_off, ra_off, cb_off, total;
+};
+
+WsLayout ws_layout(long long M, long long N, long long K) {
+  const long long Kp = k_padded(K);
+  WsLayout l;
+  l.a_off = 0;
+  l.b_off = l.a_off + align_up(static_cast<size_t>(M) * Kp * 2, kWsAlign);
+  l.ra_off = l.b_off + align_up(static_cast<size_t>(N) * Kp * 2, kWsAlign);
+  l.cb_off = l.ra_off + align_up(static_cast<size_t>(M) * 4, kWsAlign);
+  l.total = l.cb_off + align_up(static_cast<size_t>(N) * 4, kWsAlign);
+  return l;
+}
+
+// One warp per row: dst[row, k] = fp16(src[row, k] - offset) for k < K, 0 for
+// K <= k < Kp; sums[row] = sum_k (src[row, k] - offset).
+__global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(
+    const uint8_t* __restrict__ src, long long ld, int rows, int K, int Kp, int is_signed,
+    int offset, int vec, __half* __restrict__ dst, int32_t* __restrict__ sums) {
+  const int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
+  const int lane = static_cast<int>(threadIdx.x % 32);
+  if (row >= rows) return;
+  const uint8_t* s = src + static_cast<size_t>(row) * ld;
+  __half* d = dst + static_cast<size_t>(row) * Kp;
+  int32_t acc = 0;
+  if (vec) {  // K % 16 == 0, 16-byte aligned rows, Kp == K
+    for (int k = lane * 16; k < K; k += 32 * 16) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(s + k));
+      const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t out[8];
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {
+        int v[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint32_t byte = (words[wi] >> (8 * b)) & 0xFFu;
+          v[b] = (is_signed ? static_cast<int>(static_cast<int8_t>(byte)) : static_cast<int>(byte)) -
+                 offset;
+          acc += v[b];
+        }
+        __half2 h0 = __halves2half2(__int2half_rn(v[0]), __int2half_rn(v[1]));
+        __half2 h1 = __halves2half2(__int2half_rn(v[2]), __int2half_rn(v[3]));
+        out[2 * wi] = *reinterpret_cast<uint32_t*>(&h0);
+        out[2 * wi + 1] = *reinterpret_cast<uint32_t*>(&h1);
+      }
+      reinterpret_cast<uint4*>(d + k)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+      reinterpret_cast<uint4*>(d + k)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+  } else {
+    for (int k = lane; k < Kp; k += 32) {
+      int v = 0;
+      if (k < K) {
+        const uint32_t byte = s[k];
+        v = (is_signed ? static_cast<int>(static_cast<int8_t>(byte)) : static_cast<int>(byte)) -
+            offset;
+      }
+      acc += v;
+      d[k] = __int2half_rn(v);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) sums[row] = acc;
+}
+
+int launch_prepass(const void* src, long long ld, long long rows, long long K, long long Kp,
+                   int is_signed, __half* dst, int32_t* sums, cudaStream_t stream) {
+  const int offset = is_signed ? 0 : 128;
+  const int vec = (K % 16 == 0) && aligned16(src) && (ld % 16 == 0) && (Kp == K);
+  const long long blocks = (rows + 7) / 8;
+  shift_widen_rowsum_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint8_t*>(src), ld, static_cast<int>(rows), static_cast<int>(K),
+      static_cast<int>(Kp), is_signed, offset, vec, dst, sums);
+  return cudaGetLastError() == cudaSuccess ? IGC_OK : IGC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" size_t gemm_s8_zp_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  return ws_layout(M, N, K).total;
+}
+
+extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,
+                          int64_t lda, const void* Bt, int b_signed, int64_t ldb, int32_t zA,
+                          const int32_t* zA_row, int32_t zB, const int32_t* zB_col, int32_t* C32,
+                          int64_t ldc32, int8_t* C8, int64_t ldc8, float scale,
+                          const float* scale_col, void* workspace, size_t workspace_bytes,
+                          igc_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (M < 0 || N < 0 || K < 0) return IGC_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
+  if (C32 == nullptr && C8 == nullptr) return IGC_ERR_INVALID_ARG;
+  if (C32 != nullptr && ldc32 < N) return IGC_ERR_INVALID_ARG;
+  if (C8 != nullptr && ldc8 < N) return IGC_ERR_INVALID_ARG;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff) return IGC_ERR_UNSUPPORTED;
+
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != IGC_OK) return rc;
+  if (K == 0) {  // empty sum: C32 = 0 and C8 = requant(0) = 0; nothing is read
+    rc = zero_rows(C32, ldc32, M, N, 4, stream);
+    if (rc == IGC_OK) rc = zero_rows(C8, ldc8, M, N, 1, stream);
+    return rc;
+  }
+  if (A == nullptr || Bt == nullptr || lda < K || ldb < K) return IGC_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Bt) || (lda % 16) != 0 || (ldb % 16) != 0)
+    return IGC_ERR_MISALIGNED;
+  const WsLayout l = ws_layout(M, N, K);
+  if (workspace == nullptr || workspace_bytes < l.total ||
+      (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0)
+    return IGC_ERR_WORKSPACE;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __half* Ap = reinterpret_cast<__half*>(ws + l.a_off);
+  __half* Bp = reinterpret_cast<__half*>(ws + l.b_off);
+  int32_t* rA = reinterpret_cast<int32_t*>(ws + l.ra_off);
+  int32_t* cB = reinterpret_cast<int32_t*>(ws + l.cb_off);
+  const long long Kp = k_padded(K);
+
+  rc = launch_prepass(A, lda, M, K, Kp, a_signed ? 1 : 0, Ap, rA, stream);
+  if (rc != IGC_OK) return rc;
+  rc = launch_prepass(Bt, ldb, N, K, Kp, b_signed ? 1 : 0, Bp, cB, stream);
+  if (rc != IGC_OK) return rc;
+
+  CUtensorMap tmA, tmB;
+  rc = encode_tiled_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ap, Kp, M, Kp * 2, BK, BM);
+  if (rc != IGC_OK) return rc;
+  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Bp, Kp, N, Kp * 2, BK, BN);
+  if (rc != IGC_OK) return rc;
+
+  KParams p{};
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_kb = static_cast<int>((Kp + BK - 1) / BK);
+  p.chunk_kb = kIntChunkKb;
+  p.c32 = C32;
+  p.ldc32 = ldc32;
+  p.c8 = C8;
+  p.ldc8 = ldc8;
+  p.rsumA = rA;
+  p.csumB = cB;
+  p.zA = zA;
+  p.zA_row = zA_row;
+  p.zB = zB;
+  p.zB_col = zB_col;
+  p.oA = a_signed ? 0 : 128;
+  p.oB = b_signed ? 0 : 128;
+  p.scale = scale;
+  p.scale_col = scale_col;
+  p.vec_ok = vec_store_ok(C32, ldc32, 4) && vec_store_ok(C8, ldc8, 1);
+  return launch_tc_gemm<Mode::GemmInt>(dev, tmA, tmB, p, stream);
+}

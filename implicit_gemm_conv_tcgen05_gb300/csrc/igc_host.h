@@ -1,0 +1,42 @@
+// Host-side helpers shared by the entry points of libigc.so (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "igc.h"
+
+namespace igc {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  size_t smem_optin = 0;
+};
+
+// Current device's properties (cached per device).  Returns IGC_OK,
+// IGC_ERR_CUDA, or IGC_ERR_UNSUPPORTED when the device is not sm_103.
+int current_device(DeviceInfo* out);
+
+// Device address of the status word of the current device.
+unsigned long long* status_word();
+
+// Wait limit for kernels launched now.
+unsigned long long wait_limit_ns();
+
+// cuTensorMapEncodeTiled / cuTensorMapEncodeIm2col through the runtime's
+// driver entry point (the library does not link libcuda directly).
+int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                    uint32_t box_rows);
+
+int encode_im2col_nhwc(CUtensorMap* map, const void* base, int N, int H, int W, int C,
+                       int lower_h, int lower_w, int upper_h, int upper_w, uint32_t channels,
+                       uint32_t pixels, int stride_h, int stride_w);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace igc

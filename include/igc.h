@@ -1,0 +1,201 @@
+/*
+ * igc.h -- C ABI of the GB300 (sm_103a) tensor-core GEMM / implicit-GEMM
+ * convolution library (libigc.so).
+ *
+ * Pages the operations follow (cited by title and section):
+ *  [P1] "TVM在CUDA GPU上跑GEMM的全套张量化实现：WMMA/DP4A/IMMA + TensorIR调度 +
+ *       INT8/FP16多精度支持": §2.1 (tensor-core MMA with "row.col" operands: A
+ *       row-major, B column-major), §2.3 (INT8 GEMM with input zero points,
+ *       C = (A_q - zp_A)(B_q - zp_B), fused quantise / dequantise), §4.1 (the GEMM
+ *       compute definition C[i,j] = sum_k A[i,k] * B[k,j] on fp16 operands),
+ *       §4.4 (destination passing: caller-allocated inputs and outputs, mod(a, b, c)).
+ *  [P3] "如何使用 TensorCores 优化卷积" (TVM tutorial "How to optimize convolution
+ *       using TensorCores"), section "准备和算法" (3x3 convolution, zero padding
+ *       Apad, reduction over input channels and the filter window, fp16 operands
+ *       cast to float32 before the multiply-add) and "生成 CUDA 内核" (the built
+ *       function is called as func(a, w, c) on caller-owned device arrays).
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: the caller owns every buffer.  Pointers named "device" must be
+ *    device memory of the current CUDA device (e.g. torch tensors' data_ptr()).
+ *    The library allocates no device memory; gemm_s8_zp takes its scratch as a
+ *    caller-provided workspace.
+ *  - Asynchrony: compute calls enqueue work on `stream` (NULL = legacy default
+ *    stream) and return without synchronising.  A non-IGC_OK return means
+ *    nothing was enqueued (except IGC_ERR_CUDA, where a launch failed).
+ *  - Errors: no exceptions cross the ABI.  Argument errors are detected on the
+ *    host before any launch.  Kernel-side pipeline waits are bounded: if one
+ *    gives up, the kernel records it in a device status word and exits;
+ *    igc_check_device_status() reports it as IGC_ERR_DEVICE_TIMEOUT.
+ *  - Alignment: operand base pointers must be 16-byte aligned and operand row
+ *    strides (in bytes) multiples of 16 (TMA rules), else IGC_ERR_MISALIGNED.
+ *    Outputs may have any alignment; aligned outputs get vector stores.
+ *  - Device: an sm_103 GPU (GB300); any other returns IGC_ERR_UNSUPPORTED.
+ *  - Calls are stateless and re-entrant; concurrent calls on different streams
+ *    are independent (each gemm_s8_zp call needs its own workspace).
+ */
+#ifndef IGC_H
+#define IGC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *igc_stream_t;
+
+/* status codes */
+#define IGC_OK 0
+#define IGC_ERR_INVALID_ARG 1    /* null required pointer, negative size, ld < K, no output */
+#define IGC_ERR_MISALIGNED 2     /* operand pointer / row stride breaks the 16-byte TMA rules */
+#define IGC_ERR_UNSUPPORTED 3    /* shape or device outside what the kernels implement */
+#define IGC_ERR_CUDA 4           /* a CUDA runtime / driver call failed */
+#define IGC_ERR_DEVICE_TIMEOUT 5 /* a kernel's bounded pipeline wait gave up */
+#define IGC_ERR_WORKSPACE 6      /* workspace pointer null or smaller than required */
+
+/* output element types for gemm_f16 */
+#define IGC_F32 0
+#define IGC_F16 1
+
+/*
+ * gemm_f16 -- C = A * B, fp16 operands, fp32 accumulation ([P1] §4.1, §2.1).
+ *
+ *   C[i,j] = sum_{k<K} A[i,k] * Bt[j,k]      0 <= i < M, 0 <= j < N
+ *
+ *  A    device, fp16, M x K row-major, row stride lda >= K elements.
+ *  Bt   device, fp16, B stored column-major: N x K row-major (K contiguous),
+ *       row stride ldb >= K elements.
+ *  C    device, M x N row-major, row stride ldc >= N elements, element type
+ *       c_dtype: IGC_F32 (the fp32 accumulator) or IGC_F16 (round to nearest
+ *       even of the fp32 accumulator; overflow gives +-inf).  May be NULL if
+ *       C_f32_check is given.
+ *  C_f32_check  device fp32 M x N (row stride ldc32 >= N) or NULL: an extra
+ *       copy of the fp32 accumulator, so that an fp16 C can be checked as the
+ *       exact rounding of it.
+ *  Sizes: M, N, K >= 0; M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *  Alignment: A, Bt 16-byte aligned; lda, ldb multiples of 8.
+ *  Accuracy: per element |C - exact| <= 2e-3 * sum_k |A[i,k] * Bt[j,k]| (fp32
+ *  accumulation in the tensor cores, order unspecified), plus the fp16
+ *  rounding of C when c_dtype is IGC_F16.
+ */
+int gemm_f16(int64_t M, int64_t N, int64_t K,
+             const void *A, int64_t lda,
+             const void *Bt, int64_t ldb,
+             void *C, int64_t ldc, int c_dtype,
+             float *C_f32_check, int64_t ldc32,
+             igc_stream_t stream);
+
+/*
+ * gemm_s8_zp -- INT8 GEMM with input zero points and requantisation
+ * ([P1] §2.3: C = (A_q - zp_A)(B_q - zp_B) accumulated in int32, then the
+ * dequantise / requantise step of the four-term fusion).
+ *
+ *   C32[i,j] = sum_{k<K} (A_q[i,k] - zA_i) * (B_q[k,j] - zB_j)     (int32, wraps mod 2^32)
+ *   C8[i,j]  = clamp(rne(fp32(C32[i,j]) * scale_j), -128, 127)
+ *
+ *  A       device, M x K row-major bytes, uint8 (a_signed = 0) or int8 (a_signed = 1),
+ *          row stride lda >= K bytes.
+ *  Bt      device, B stored column-major: N x K row-major bytes, uint8 or int8
+ *          (b_signed), row stride ldb >= K bytes.
+ *  zA      per-tensor zero point of A, used when zA_row is NULL.
+ *  zA_row  device int32[M] per-row zero points, or NULL.
+ *  zB      per-tensor zero point of B, used when zB_col is NULL.
+ *  zB_col  device int32[N] per-column zero points, or NULL.
+ *  C32     device int32 M x N row-major (row stride ldc32 >= N), or NULL.
+ *  C8      device int8 M x N row-major (row stride ldc8 >= N), or NULL.  At
+ *          least one of C32 / C8 must be given.
+ *  scale   per-tensor fp32 scale, used when scale_col is NULL.
+ *  scale_col  device fp32[N] per-column scales, or NULL.
+ *  workspace  device scratch of at least gemm_s8_zp_workspace_size(M, N, K)
+ *          bytes, 256-byte aligned, owned by the caller, not shared with a
+ *          concurrent call.  It holds the operands shifted to [-128, 127] and
+ *          widened to fp16, and their row / column sums.
+ *  Rounding: fp32(C32) rounds to nearest even; the product is one fp32
+ *  multiply rounded to nearest even; the integer rounding is half-to-even; a
+ *  NaN product gives 0.  Results are bit-exact (no tolerance).
+ *  Sizes: M, N, K >= 0; M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *  Alignment: A, Bt 16-byte aligned; lda, ldb multiples of 16.
+ */
+int gemm_s8_zp(int64_t M, int64_t N, int64_t K,
+               const void *A, int a_signed, int64_t lda,
+               const void *Bt, int b_signed, int64_t ldb,
+               int32_t zA, const int32_t *zA_row,
+               int32_t zB, const int32_t *zB_col,
+               int32_t *C32, int64_t ldc32,
+               int8_t *C8, int64_t ldc8,
+               float scale, const float *scale_col,
+               void *workspace, size_t workspace_bytes,
+               igc_stream_t stream);
+
+/* Bytes of workspace gemm_s8_zp needs for an M x N x K problem (0 if any size < 0). */
+size_t gemm_s8_zp_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * conv2d_nhwc_f16_implicit -- 2-D convolution (cross-correlation, no kernel
+ * flip) as an implicit GEMM ([P3] "准备和算法"): no im2col tensor is built;
+ * the A operand is gathered by TMA in im2col mode.
+ *
+ *   y[n,p,q,k] = sum_{r<R} sum_{s<S} sum_{c<C}
+ *                xpad(n, p*stride_h + r - pad_h, q*stride_w + s - pad_w, c) * w[k,r,s,c]
+ *
+ *  with xpad = x inside [0,H) x [0,W) and 0 outside (zero padding), fp32
+ *  accumulation, P = (H + 2*pad_h - R)/stride_h + 1, Q likewise.
+ *
+ *  x    device fp16 NHWC, N x H x W x C, dense.
+ *  w    device fp16 KRSC, K x R x S x C, dense (= a K x (R*S*C) K-major matrix).
+ *  y    device fp16 NHWC (N x P x Q x K), dense, round to nearest even.  May be
+ *       NULL if y_f32_check is given.
+ *  y_f32_check  device fp32 N x P x Q x K or NULL: copy of the fp32 accumulator.
+ *  Supported: C a multiple of 8 (16-byte pixel rows), stride_h = stride_w = 1,
+ *  1 <= R, S <= 8, 0 <= pad <= 7 with pad <= R-1 (S-1), dense tensors,
+ *  N*H*W*C < 2^31 and N*P*Q*K < 2^31; else IGC_ERR_UNSUPPORTED.
+ *  N == 0 is a no-op.  Accuracy as for gemm_f16 with the sum over the taps.
+ */
+int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R, int S,
+                             int pad_h, int pad_w, int stride_h, int stride_w,
+                             const void *x, const void *w,
+                             void *y, float *y_f32_check,
+                             igc_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *igc_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns IGC_OK, IGC_ERR_DEVICE_TIMEOUT if a kernel's
+ * bounded wait gave up since the last check (details via
+ * igc_last_device_status()), or IGC_ERR_CUDA if the synchronisation failed.
+ */
+int igc_check_device_status(igc_stream_t stream);
+
+/* Raw status word read by the last igc_check_device_status() call:
+ * (code << 56) | (wait site << 32) | block index; 0 when none. */
+uint64_t igc_last_device_status(void);
+
+/*
+ * Limit, in nanoseconds, of every kernel-side pipeline wait launched after
+ * this call (default 2e9; values < 1000 are raised to 1000).  Returns the
+ * previous limit.  Process-wide.
+ */
+uint64_t igc_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Diagnostic: launches one CTA that waits on an mbarrier nothing ever
+ * completes, with the current wait limit, and returns.  The wait gives up
+ * after the limit and records IGC_ERR_DEVICE_TIMEOUT for
+ * igc_check_device_status(); the context stays usable.  Used to test the
+ * failure path without faulting or hanging the GPU.
+ */
+int igc_debug_wait_timeout_probe(igc_stream_t stream);
+
+/* Library version, "major.minor.patch". */
+const char *igc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IGC_H */

@@ -1,0 +1,92 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds, loads,
+exports every function include/igc.h declares, and rejects bad arguments on
+the host before touching a device."""
+
+import ctypes
+import re
+
+import pytest
+
+import implicit_gemm_conv_tcgen05_gb300 as igc
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    L = igc.lib()
+    names = igc.declared_functions()
+    expected = {"gemm_f16", "gemm_s8_zp", "gemm_s8_zp_workspace_size", "conv2d_nhwc_f16_implicit",
+                "igc_status_string", "igc_check_device_status", "igc_last_device_status",
+                "igc_set_wait_limit_ns", "igc_debug_wait_timeout_probe", "igc_version"}
+    assert expected <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+        assert ctypes.cast(getattr(L, n), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version():
+    for code in range(7):
+        s = igc.status_string(code)
+        assert s and s != "unknown status"
+    assert igc.status_string(99) == "unknown status"
+    assert re.fullmatch(r"\d+\.\d+\.\d+", igc.igc_version())
+
+
+def test_workspace_size_arithmetic():
+    # A' (M x Kp fp16) + B' (N x Kp fp16) + row sums + column sums, each 256-aligned
+    def up(v):
+        return (v + 255) // 256 * 256
+    for M, N, K in [(1024, 1024, 1024), (8192, 8192, 8192), (3, 5, 7), (1, 1, 1)]:
+        Kp = (K + 7) // 8 * 8
+        want = up(M * Kp * 2) + up(N * Kp * 2) + up(4 * M) + up(4 * N)
+        assert igc.gemm_s8_zp_workspace_size(M, N, K) == want
+    assert igc.gemm_s8_zp_workspace_size(-1, 2, 3) == 0
+
+
+def test_wait_limit_setter_roundtrip():
+    old = igc.igc_set_wait_limit_ns(5_000_000)
+    assert igc.igc_set_wait_limit_ns(10) == 5_000_000      # returns the previous value
+    assert igc.igc_set_wait_limit_ns(old) == 1000          # raised to the 1 us floor
+    assert igc.igc_set_wait_limit_ns(old) == old
+
+
+def test_host_validation_before_any_device_call():
+    L = igc.lib()
+    dummy = ctypes.c_void_p(4096)
+    # negative sizes, bad output type, no outputs: rejected on the host
+    assert L.gemm_f16(-1, 4, 4, dummy, 4, dummy, 4, dummy, 4, 0, None, 0, None) == igc.IGC_ERR_INVALID_ARG
+    assert L.gemm_f16(4, 4, 4, dummy, 4, dummy, 4, dummy, 4, 7, None, 0, None) == igc.IGC_ERR_INVALID_ARG
+    assert L.gemm_f16(4, 4, 4, dummy, 4, dummy, 4, None, 0, 0, None, 0, None) == igc.IGC_ERR_INVALID_ARG
+    assert L.gemm_f16(4, 4, 4, dummy, 4, dummy, 4, dummy, 3, 0, None, 0, None) == igc.IGC_ERR_INVALID_ARG
+    # empty problems are a no-op, even with null operands and outputs (empty tensors)
+    assert L.gemm_f16(0, 8, 16, None, 16, None, 16, None, 8, 0, None, 0, None) == igc.IGC_OK
+    assert L.gemm_f16(8, 0, 16, None, 16, None, 16, None, 0, 1, None, 0, None) == igc.IGC_OK
+    assert L.gemm_s8_zp(0, 8, 16, None, 0, 16, None, 0, 16, 0, None, 0, None,
+                        None, 8, None, 8, 1.0, None, None, 0, None) == igc.IGC_OK
+    assert L.conv2d_nhwc_f16_implicit(0, 4, 4, 8, 8, 3, 3, 1, 1, 1, 1, None, None, None, None,
+                                      None) == igc.IGC_OK
+    assert L.gemm_f16(0, 4, 4, None, 4, None, 4, dummy, 4, 0, None, 0, None) == igc.IGC_OK
+    assert L.gemm_f16(4, 0, 4, None, 4, None, 4, dummy, 4, 0, None, 0, None) == igc.IGC_OK
+    assert L.gemm_s8_zp(-3, 4, 4, dummy, 0, 16, dummy, 0, 16, 0, None, 0, None,
+                        dummy, 4, None, 0, 1.0, None, None, 0, None) == igc.IGC_ERR_INVALID_ARG
+    assert L.gemm_s8_zp(4, 4, 4, dummy, 0, 16, dummy, 0, 16, 0, None, 0, None,
+                        None, 0, None, 0, 1.0, None, None, 0, None) == igc.IGC_ERR_INVALID_ARG
+    assert L.gemm_s8_zp(0, 4, 4, None, 0, 16, None, 0, 16, 0, None, 0, None,
+                        dummy, 4, None, 0, 1.0, None, None, 0, None) == igc.IGC_OK
+    conv = L.conv2d_nhwc_f16_implicit
+    assert conv(1, 14, 14, 256, 512, 3, 3, -1, 1, 1, 1, dummy, dummy, dummy, None, None) == igc.IGC_ERR_INVALID_ARG
+    assert conv(1, 2, 2, 8, 8, 5, 5, 0, 0, 1, 1, dummy, dummy, dummy, None, None) == igc.IGC_ERR_INVALID_ARG
+    assert conv(1, 14, 14, 256, 512, 3, 3, 1, 1, 1, 1, dummy, dummy, None, None, None) == igc.IGC_ERR_INVALID_ARG
+    assert conv(0, 14, 14, 256, 512, 3, 3, 1, 1, 1, 1, None, None, dummy, None, None) == igc.IGC_OK
+    # stride and channel-count limits are reported as unsupported before any device call
+    assert conv(1, 14, 14, 256, 512, 3, 3, 1, 1, 2, 2, dummy, dummy, dummy, None, None) == igc.IGC_ERR_UNSUPPORTED
+    assert conv(1, 14, 14, 12, 512, 3, 3, 1, 1, 1, 1, dummy, dummy, dummy, None, None) == igc.IGC_ERR_UNSUPPORTED
+
+
+def test_header_declares_c_linkage_and_statuses():
+    with open(igc.HEADER) as f:
+        text = f.read()
+    assert 'extern "C"' in text
+    for name, code in [("IGC_OK", 0), ("IGC_ERR_INVALID_ARG", 1), ("IGC_ERR_MISALIGNED", 2),
+                       ("IGC_ERR_UNSUPPORTED", 3), ("IGC_ERR_CUDA", 4), ("IGC_ERR_DEVICE_TIMEOUT", 5),
+                       ("IGC_ERR_WORKSPACE", 6)]:
+        assert re.search(rf"#define {name} {code}\b", text)
+        assert getattr(igc, name) == code
