@@ -1,0 +1,437 @@
+"""Benchmark of the GEMM / implicit-GEMM convolution hot path on GB300.
+
+One step = one pass of every operation of the path over its headline
+synthetic workload, inputs resident in HBM:
+  * fp16 GEMM 4096^3, A row-major, B column-major, N(0,1), fp16 C  (137.4 GFLOP)
+  * 3x3 conv, NHWC 256x14x14x256 -> 512, pad 1, stride 1, fp16     (118.4 GFLOP nominal)
+  * int8 GEMM 8192^3, uint8 A with per-row zero points, int8 B, per-column
+    fp32 scales, fused zero-point correction + requantisation to int8
+    (1.100 TOP): operand pre-pass + tcgen05 GEMM
+`value` = dense tensor operations of the step (FP16 FLOPs + INT8 OPs) per
+second, summed over ranks.  L2 is flushed (256 MiB write, untimed) before
+every timed step; each step is timed with CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (the plain reference implementation of
+the same operations) on the host cores, a bounded sample of the step per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "TFLOPS (FP16) / TOPS (INT8) per shape, device-timed, and % of GB300 dense peak"
+UNIT = "T(FL)OP/s"
+WORKLOAD = ("one pass of the hot path: fp16 GEMM 4096^3 (fp16 out) + 3x3 conv NHWC "
+            "256x14x14x256->512 pad 1 (fp16 out) + int8 zero-point GEMM 8192^3 (per-row zA, "
+            "per-column scale, int8 out)")
+OPS = {
+    "gemm_f16_4096": 2.0 * 4096 ** 3,
+    "conv3x3_256x14x14x256_512": 2.0 * 256 * 14 * 14 * 512 * 3 * 3 * 256,
+    "gemm_s8_zp_8192": 2.0 * 8192 ** 3,
+}
+OPS_PER_STEP = sum(OPS.values())
+FALLBACK_TFLOPS = 1900.0
+KERNEL_SOURCES = os.path.join(ROOT, "implicit_gemm_conv_tcgen05_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(KERNEL_SOURCES)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(KERNEL_SOURCES, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            float(d.get("hbm_gbs", 0.0)), "measured"
+    return FALLBACK_TFLOPS, 1700.0, 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def make_inputs():
+    w3, w4, w5 = synth.workload(3), synth.workload(4), synth.workload(5)
+    return w3, w4, w5
+
+
+class Step:
+    """Device-resident buffers of one step and the calls that make it."""
+
+    def __init__(self, w3, w4, w5, device):
+        import torch
+        import implicit_gemm_conv_tcgen05_gb300 as igc
+        self.igc = igc
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        self.A3, self.B3 = t(w3["A"]), t(w3["Bt"])
+        self.C3 = torch.empty((4096, 4096), dtype=torch.float16, device=device)
+        self.x, self.w = t(w4["x"]), t(w4["w"])
+        self.y = torch.empty((256, 14, 14, 512), dtype=torch.float16, device=device)
+        self.Aq, self.Bq = t(w5["A"]), t(w5["Bt"])
+        self.zA = t(w5["zA_row"])
+        self.sc = t(w5["scale_col"])
+        self.C8 = torch.empty((8192, 8192), dtype=torch.int8, device=device)
+        self.ws = torch.empty(igc.gemm_s8_zp_workspace_size(8192, 8192, 8192), dtype=torch.uint8,
+                              device=device)
+        self.launches_per_step = 5  # gemm_f16, conv, 2 x int8 pre-pass, int8 GEMM
+
+    def run(self, ev=None):
+        igc = self.igc
+        if ev is not None:
+            ev[0].record()
+        igc.gemm_f16(self.A3, self.B3, self.C3)
+        if ev is not None:
+            ev[1].record()
+        igc.conv2d_nhwc_f16_implicit(self.x, self.w, self.y, pad=(1, 1))
+        if ev is not None:
+            ev[2].record()
+        igc.gemm_s8_zp_prepare(self.Aq, self.Bq, self.ws)
+        if ev is not None:
+            ev[3].record()
+        igc.gemm_s8_zp_run(8192, 8192, 8192, 0, 1, self.ws, zA_row=self.zA, C8=self.C8,
+                           scale_col=self.sc)
+        if ev is not None:
+            ev[4].record()
+
+
+def e2e_measure(step: "Step", w3, w4, w5, steps: int):
+    """Same step through the public API from pinned host buffers: every step copies its
+    inputs host->device and its results device->host inside the timed region."""
+    import torch
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_in = [(pin(w3["A"]), step.A3), (pin(w3["Bt"]), step.B3), (pin(w4["x"]), step.x),
+            (pin(w4["w"]), step.w), (pin(w5["A"]), step.Aq), (pin(w5["Bt"]), step.Bq),
+            (pin(w5["zA_row"]), step.zA), (pin(w5["scale_col"]), step.sc)]
+    h_out = [(torch.empty(d.shape, dtype=d.dtype).pin_memory(), d) for d in (step.C3, step.y, step.C8)]
+    h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
+    d2h = sum(h.numel() * h.element_size() for h, _ in h_out)
+
+    def one():
+        for h, d in h_in:
+            d.copy_(h, non_blocking=True)
+        step.run()
+        for h, d in h_out:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    e.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch of `kernel_key` from the committed ncu summary, if the
+    kernel sources have not changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("csrc_sha256_16") != csrc_digest():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    import implicit_gemm_conv_tcgen05_gb300 as igc
+    igc.lib()
+
+    t0 = time.time()
+    w3, w4, w5 = make_inputs()
+    log(f"[bench] inputs generated in {time.time() - t0:.1f}s")
+    step = Step(w3, w4, w5, device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    rc = igc.igc_check_device_status()
+    if rc != igc.IGC_OK:
+        raise RuntimeError(f"device status after warm-up: {igc.status_string(rc)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()
+        step.run(evs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    rc = igc.igc_check_device_status()
+    if rc != igc.IGC_OK:
+        raise RuntimeError(f"device status after timing: {igc.status_string(rc)}")
+
+    seg = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in evs])  # ms
+    step_ms = seg.sum(axis=1)
+    ms_local = float(step_ms.mean())
+    ms = ms_local
+    if world > 1:
+        tt = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * OPS_PER_STEP / (ms * 1e-3) / 1e12
+
+    peak_burst, peak_sust, hbm, peak_kind = measured_peaks()
+    f16_ms, conv_ms, prep_ms, run_ms = (float(v) for v in seg.mean(axis=0))
+    per_shape = {
+        "gemm_f16_4096^3": {"ms": f16_ms, "tflops": OPS["gemm_f16_4096"] / f16_ms / 1e9},
+        "conv3x3_256x14x14x256->512": {"ms": conv_ms,
+                                       "tflops": OPS["conv3x3_256x14x14x256_512"] / conv_ms / 1e9},
+        "gemm_s8_zp_8192^3": {"ms": prep_ms + run_ms,
+                              "tops": OPS["gemm_s8_zp_8192"] / (prep_ms + run_ms) / 1e9,
+                              "prepass_ms": prep_ms, "gemm_kernel_ms": run_ms,
+                              "gemm_kernel_tops": OPS["gemm_s8_zp_8192"] / run_ms / 1e9},
+    }
+    for k, v in per_shape.items():
+        t = v.get("tflops", v.get("tops"))
+        v["frac_of_peak"] = t / peak_burst
+    achieved = OPS["gemm_s8_zp_8192"] / (run_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst, "traffic": traffic_for("gemm_s8_zp_run_8192"),
+                "kernel": "igc_tc_gemm_kernel<GemmInt> (int8 8192^3 on the fp16 tensor pipe)",
+                "peak_source": f"{peak_kind} bf16 burst (fp16 rate = bf16 rate)"}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": WORKLOAD, "l2": "flushed before every step (256 MiB write, untimed)",
+                   "ops_per_step": OPS_PER_STEP, "parallelism": f"replicas x{world}",
+                   "int8_path": "exact integer GEMM on the kind::f16 tensor pipe"},
+        "per_shape": per_shape, "roofline": roofline, "clocks": clk,
+        "gpu_launches": step.launches_per_step * args.steps,
+    }
+
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        e_ms, h2d, d2h = e2e_measure(step, w3, w4, w5, e2e_steps)
+        e_local = e_ms
+        if world > 1:
+            tt = torch.tensor([e_local], dtype=torch.float64, device=device)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        result["e2e"] = {"value": world * OPS_PER_STEP / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+                         "ms_per_step": e_ms, "steps": e2e_steps,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w3, w4, w5, target_s=args.cpu_seconds)
+    return result
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w3, w4, w5, frac_log2: int):
+    """Runs the oracle on 2^-frac_log2 of each operation of the step (rows of the
+    GEMMs, images of the convolution); returns (ops, seconds, description)."""
+    import oracle
+    f = 2.0 ** -frac_log2
+    r3 = max(1, int(round(4096 * f)))
+    n4 = max(1, int(round(256 * f)))
+    r5 = max(1, int(round(8192 * f)))
+    t0 = time.perf_counter()
+    oracle.gemm_f16(w3["A"][:r3], w3["Bt"])
+    oracle.conv2d_nhwc_f16(w4["x"][:n4], w4["w"], pad=(1, 1))
+    oracle.gemm_s8_zp(w5["A"][:r5], w5["Bt"], a_signed=0, b_signed=1, zA_row=w5["zA_row"][:r5],
+                      scale_col=w5["scale_col"])
+    dt = time.perf_counter() - t0
+    ops = 2.0 * r3 * 4096 * 4096 + 2.0 * n4 * 14 * 14 * 512 * 9 * 256 + 2.0 * r5 * 8192 * 8192
+    desc = (f"{r3} of 4096 fp16-GEMM rows, {n4} of 256 conv images, {r5} of 8192 int8-GEMM rows "
+            f"(the same inputs)")
+    return ops, dt, desc
+
+
+def cpu_baseline(w3, w4, w5, target_s: float = 15.0):
+    import oracle
+    k = 10
+    ops, dt, desc = oracle_sample(w3, w4, w5, k)
+    while dt < target_s / 2 and k > 1:
+        # each step halves k's fraction exponent by the measured shortfall
+        k = max(1, k - max(1, int(np.floor(np.log2(target_s / max(dt, 1e-3))))))
+        ops, dt, desc = oracle_sample(w3, w4, w5, k)
+    return {"value": ops / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle", "sample": desc, "seconds": dt}
+
+
+def run_reference(args):
+    import oracle
+    t0 = time.time()
+    w3, w4, w5 = make_inputs()
+    log(f"[bench] inputs generated in {time.time() - t0:.1f}s")
+    # per-step sample sized so that warm-up + steps take about two minutes
+    k = 12
+    ops, dt, desc = oracle_sample(w3, w4, w5, k)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    while dt * 2 < budget and k > 6:
+        k -= 1
+        ops, dt, desc = oracle_sample(w3, w4, w5, k)
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_sample(w3, w4, w5, k)
+    times = []
+    for _ in range(args.steps):
+        ops, dt, desc = oracle_sample(w3, w4, w5, k)
+        times.append(dt)
+    ms = 1e3 * float(np.mean(times))
+    value = ops / (ms * 1e-3) / 1e12
+    cores = oracle.default_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64/int64 (oracle)",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": WORKLOAD, "sample_per_step": desc, "ops_per_sample": ops},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        result = run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

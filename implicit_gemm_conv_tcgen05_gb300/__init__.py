@@ -62,6 +62,12 @@ def lib() -> ctypes.CDLL:
                                      ctypes.c_int32, vp, ctypes.c_int32, vp,
                                      vp, i64, vp, i64, ctypes.c_float, vp, vp, sz, vp]
             L.gemm_s8_zp.restype = i32
+            L.gemm_s8_zp_prepare.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64, vp, sz, vp]
+            L.gemm_s8_zp_prepare.restype = i32
+            L.gemm_s8_zp_run.argtypes = [i64, i64, i64, i32, i32, ctypes.c_int32, vp,
+                                         ctypes.c_int32, vp, vp, i64, vp, i64, ctypes.c_float,
+                                         vp, vp, sz, vp]
+            L.gemm_s8_zp_run.restype = i32
             L.gemm_s8_zp_workspace_size.argtypes = [i64, i64, i64]
             L.gemm_s8_zp_workspace_size.restype = sz
             L.conv2d_nhwc_f16_implicit.argtypes = [i32] * 11 + [vp, vp, vp, vp, vp]
@@ -217,6 +223,41 @@ def gemm_s8_zp(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, C32=None, C8=None,
                           _ptr(workspace), workspace.numel() * workspace.element_size(),
                           _stream(stream))
     _check(rc, "gemm_s8_zp")
+    return C32, C8
+
+
+def gemm_s8_zp_prepare(A, Bt, workspace, M=None, N=None, K=None, stream=None):
+    """Operand pre-pass of gemm_s8_zp into `workspace`; A or Bt may be None to keep
+    the prepared copy of that operand (M, N, K must then be given)."""
+    import torch
+    lda = ldb = 0
+    a_signed = b_signed = 0
+    if A is not None:
+        M, K, lda = _rows(A, "A", (torch.uint8, torch.int8))
+        a_signed = 1 if A.dtype == torch.int8 else 0
+    if Bt is not None:
+        N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8))
+        if K is not None and K2 != K:
+            raise ValueError("A and Bt disagree on K")
+        K = K2
+        b_signed = 1 if Bt.dtype == torch.int8 else 0
+    rc = lib().gemm_s8_zp_prepare(M, N, K, _ptr(A), a_signed, lda, _ptr(Bt), b_signed, ldb,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    _check(rc, "gemm_s8_zp_prepare")
+
+
+def gemm_s8_zp_run(M, N, K, a_signed, b_signed, workspace, zA=0, zA_row=None, zB=0, zB_col=None,
+                   C32=None, C8=None, scale=0.0, scale_col=None, stream=None):
+    """tcgen05 GEMM + fused zero-point correction / requantisation over a prepared workspace."""
+    ldc32 = C32.stride(0) if C32 is not None else 0
+    ldc8 = C8.stride(0) if C8 is not None else 0
+    rc = lib().gemm_s8_zp_run(M, N, K, int(a_signed), int(b_signed), int(zA), _ptr(zA_row),
+                              int(zB), _ptr(zB_col), _ptr(C32), max(ldc32, N if C32 is not None else 0),
+                              _ptr(C8), max(ldc8, N if C8 is not None else 0), float(scale),
+                              _ptr(scale_col), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "gemm_s8_zp_run")
     return C32, C8
 
 

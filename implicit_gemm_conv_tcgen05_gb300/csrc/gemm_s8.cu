@@ -112,52 +112,90 @@ extern "C" size_t gemm_s8_zp_workspace_size(int64_t M, int64_t N, int64_t K) {
   return ws_layout(M, N, K).total;
 }
 
-extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,
-                          int64_t lda, const void* Bt, int b_signed, int64_t ldb, int32_t zA,
-                          const int32_t* zA_row, int32_t zB, const int32_t* zB_col, int32_t* C32,
-                          int64_t ldc32, int8_t* C8, int64_t ldc8, float scale,
-                          const float* scale_col, void* workspace, size_t workspace_bytes,
-                          igc_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+namespace {
+
+// Checks shared by the three entry points; returns IGC_OK or a status.
+int check_common(int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return IGC_ERR_INVALID_ARG;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff) return IGC_ERR_UNSUPPORTED;
+  return IGC_OK;
+}
+
+int check_workspace(const void* workspace, size_t bytes, const WsLayout& l) {
+  if (workspace == nullptr || bytes < l.total ||
+      (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0)
+    return IGC_ERR_WORKSPACE;
+  return IGC_OK;
+}
+
+}  // namespace
+
+extern "C" int gemm_s8_zp_prepare(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,
+                                  int64_t lda, const void* Bt, int b_signed, int64_t ldb,
+                                  void* workspace, size_t workspace_bytes, igc_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int rc = check_common(M, N, K);
+  if (rc != IGC_OK) return rc;
+  if (A == nullptr && Bt == nullptr) return IGC_ERR_INVALID_ARG;
+  if (M == 0 || N == 0 || K == 0) return IGC_OK;  // nothing to prepare
+  if ((A != nullptr && lda < K) || (Bt != nullptr && ldb < K)) return IGC_ERR_INVALID_ARG;
+  if ((A != nullptr && (!aligned16(A) || lda % 16 != 0)) ||
+      (Bt != nullptr && (!aligned16(Bt) || ldb % 16 != 0)))
+    return IGC_ERR_MISALIGNED;
+  const WsLayout l = ws_layout(M, N, K);
+  rc = check_workspace(workspace, workspace_bytes, l);
+  if (rc != IGC_OK) return rc;
+  DeviceInfo dev;
+  rc = current_device(&dev);
+  if (rc != IGC_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const long long Kp = k_padded(K);
+  if (A != nullptr) {
+    rc = launch_prepass(A, lda, M, K, Kp, a_signed ? 1 : 0,
+                        reinterpret_cast<__half*>(ws + l.a_off),
+                        reinterpret_cast<int32_t*>(ws + l.ra_off), stream);
+    if (rc != IGC_OK) return rc;
+  }
+  if (Bt != nullptr) {
+    rc = launch_prepass(Bt, ldb, N, K, Kp, b_signed ? 1 : 0,
+                        reinterpret_cast<__half*>(ws + l.b_off),
+                        reinterpret_cast<int32_t*>(ws + l.cb_off), stream);
+    if (rc != IGC_OK) return rc;
+  }
+  return IGC_OK;
+}
+
+extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
+                              int32_t zA, const int32_t* zA_row, int32_t zB,
+                              const int32_t* zB_col, int32_t* C32, int64_t ldc32, int8_t* C8,
+                              int64_t ldc8, float scale, const float* scale_col,
+                              const void* workspace, size_t workspace_bytes,
+                              igc_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int rc = check_common(M, N, K);
+  if (rc != IGC_OK) return rc;
   if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
   if (C32 == nullptr && C8 == nullptr) return IGC_ERR_INVALID_ARG;
   if (C32 != nullptr && ldc32 < N) return IGC_ERR_INVALID_ARG;
   if (C8 != nullptr && ldc8 < N) return IGC_ERR_INVALID_ARG;
-  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff) return IGC_ERR_UNSUPPORTED;
-
   DeviceInfo dev;
-  int rc = current_device(&dev);
+  rc = current_device(&dev);
   if (rc != IGC_OK) return rc;
   if (K == 0) {  // empty sum: C32 = 0 and C8 = requant(0) = 0; nothing is read
     rc = zero_rows(C32, ldc32, M, N, 4, stream);
     if (rc == IGC_OK) rc = zero_rows(C8, ldc8, M, N, 1, stream);
     return rc;
   }
-  if (A == nullptr || Bt == nullptr || lda < K || ldb < K) return IGC_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(Bt) || (lda % 16) != 0 || (ldb % 16) != 0)
-    return IGC_ERR_MISALIGNED;
   const WsLayout l = ws_layout(M, N, K);
-  if (workspace == nullptr || workspace_bytes < l.total ||
-      (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0)
-    return IGC_ERR_WORKSPACE;
+  rc = check_workspace(workspace, workspace_bytes, l);
+  if (rc != IGC_OK) return rc;
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  __half* Ap = reinterpret_cast<__half*>(ws + l.a_off);
-  __half* Bp = reinterpret_cast<__half*>(ws + l.b_off);
-  int32_t* rA = reinterpret_cast<int32_t*>(ws + l.ra_off);
-  int32_t* cB = reinterpret_cast<int32_t*>(ws + l.cb_off);
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   const long long Kp = k_padded(K);
-
-  rc = launch_prepass(A, lda, M, K, Kp, a_signed ? 1 : 0, Ap, rA, stream);
-  if (rc != IGC_OK) return rc;
-  rc = launch_prepass(Bt, ldb, N, K, Kp, b_signed ? 1 : 0, Bp, cB, stream);
-  if (rc != IGC_OK) return rc;
-
   CUtensorMap tmA, tmB;
-  rc = encode_tiled_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ap, Kp, M, Kp * 2, BK, BM);
+  rc = encode_tiled_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws + l.a_off, Kp, M, Kp * 2, BK, BM);
   if (rc != IGC_OK) return rc;
-  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Bp, Kp, N, Kp * 2, BK, BN);
+  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws + l.b_off, Kp, N, Kp * 2, BK, BN);
   if (rc != IGC_OK) return rc;
 
   KParams p{};
@@ -170,8 +208,8 @@ extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_
   p.ldc32 = ldc32;
   p.c8 = C8;
   p.ldc8 = ldc8;
-  p.rsumA = rA;
-  p.csumB = cB;
+  p.rsumA = reinterpret_cast<const int32_t*>(ws + l.ra_off);
+  p.csumB = reinterpret_cast<const int32_t*>(ws + l.cb_off);
   p.zA = zA;
   p.zA_row = zA_row;
   p.zB = zB;
@@ -182,4 +220,25 @@ extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_
   p.scale_col = scale_col;
   p.vec_ok = vec_store_ok(C32, ldc32, 4) && vec_store_ok(C8, ldc8, 1);
   return launch_tc_gemm<Mode::GemmInt>(dev, tmA, tmB, p, stream);
+}
+
+extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,
+                          int64_t lda, const void* Bt, int b_signed, int64_t ldb, int32_t zA,
+                          const int32_t* zA_row, int32_t zB, const int32_t* zB_col, int32_t* C32,
+                          int64_t ldc32, int8_t* C8, int64_t ldc8, float scale,
+                          const float* scale_col, void* workspace, size_t workspace_bytes,
+                          igc_stream_t stream) {
+  int rc = check_common(M, N, K);
+  if (rc != IGC_OK) return rc;
+  if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
+  if (C32 == nullptr && C8 == nullptr) return IGC_ERR_INVALID_ARG;
+  if ((C32 != nullptr && ldc32 < N) || (C8 != nullptr && ldc8 < N)) return IGC_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (A == nullptr || Bt == nullptr) return IGC_ERR_INVALID_ARG;
+    rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,
+                            workspace_bytes, stream);
+    if (rc != IGC_OK) return rc;
+  }
+  return gemm_s8_zp_run(M, N, K, a_signed, b_signed, zA, zA_row, zB, zB_col, C32, ldc32, C8,
+                        ldc8, scale, scale_col, workspace, workspace_bytes, stream);
 }

@@ -134,6 +134,38 @@ int gemm_s8_zp(int64_t M, int64_t N, int64_t K,
 size_t gemm_s8_zp_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
+ * gemm_s8_zp is these two phases in sequence; they are exported so that a
+ * caller can prepare a constant operand (e.g. quantised weights Bt) once and
+ * reuse it, and so that each phase can be timed on its own.
+ *
+ * gemm_s8_zp_prepare -- the operand pre-pass: for each non-NULL operand,
+ * writes its values shifted to [-128, 127] (minus 128 for uint8, unchanged
+ * for int8) as fp16 into the workspace, with the row sums of the shifted
+ * values.  A == NULL keeps the workspace's prepared A; Bt == NULL keeps B.
+ * At least one must be non-NULL.  Arguments as for gemm_s8_zp; the
+ * workspace must be sized for the same (M, N, K).
+ *
+ * gemm_s8_zp_run -- the tcgen05 GEMM over the prepared workspace with the
+ * fused zero-point correction and requantisation; a_signed / b_signed must
+ * be those the operands were prepared with.  Outputs and rounding as for
+ * gemm_s8_zp.  The workspace is only read.
+ */
+int gemm_s8_zp_prepare(int64_t M, int64_t N, int64_t K,
+                       const void *A, int a_signed, int64_t lda,
+                       const void *Bt, int b_signed, int64_t ldb,
+                       void *workspace, size_t workspace_bytes,
+                       igc_stream_t stream);
+
+int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
+                   int32_t zA, const int32_t *zA_row,
+                   int32_t zB, const int32_t *zB_col,
+                   int32_t *C32, int64_t ldc32,
+                   int8_t *C8, int64_t ldc8,
+                   float scale, const float *scale_col,
+                   const void *workspace, size_t workspace_bytes,
+                   igc_stream_t stream);
+
+/*
  * conv2d_nhwc_f16_implicit -- 2-D convolution (cross-correlation, no kernel
  * flip) as an implicit GEMM ([P3] "准备和算法"): no im2col tensor is built;
  * the A operand is gathered by TMA in im2col mode.

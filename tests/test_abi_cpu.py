@@ -13,7 +13,8 @@ import implicit_gemm_conv_tcgen05_gb300 as igc
 def test_library_loads_and_exports_every_declared_symbol():
     L = igc.lib()
     names = igc.declared_functions()
-    expected = {"gemm_f16", "gemm_s8_zp", "gemm_s8_zp_workspace_size", "conv2d_nhwc_f16_implicit",
+    expected = {"gemm_f16", "gemm_s8_zp", "gemm_s8_zp_workspace_size", "gemm_s8_zp_prepare",
+                "gemm_s8_zp_run", "conv2d_nhwc_f16_implicit",
                 "igc_status_string", "igc_check_device_status", "igc_last_device_status",
                 "igc_set_wait_limit_ns", "igc_debug_wait_timeout_probe", "igc_version"}
     assert expected <= set(names)
