@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_int32, vp, vp, i64, vp, i64, ctypes.c_float,
                                          vp, vp, sz, vp]
             L.gemm_s8_zp_run.restype = i32
+            L.gemm_s8_zp_noalloc.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64,
+                                             ctypes.c_int32, vp, ctypes.c_int32, vp,
+                                             vp, i64, vp, i64, ctypes.c_float, vp, vp]
+            L.gemm_s8_zp_noalloc.restype = i32
             L.gemm_s8_zp_workspace_size.argtypes = [i64, i64, i64]
             L.gemm_s8_zp_workspace_size.restype = sz
             L.conv2d_nhwc_f16_implicit.argtypes = [i32] * 11 + [vp, vp, vp, vp, vp]
@@ -223,6 +227,30 @@ def gemm_s8_zp(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, C32=None, C8=None,
                           _ptr(workspace), workspace.numel() * workspace.element_size(),
                           _stream(stream))
     _check(rc, "gemm_s8_zp")
+    return C32, C8
+
+
+IGC_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def gemm_s8_zp_noalloc(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, C32=None, C8=None,
+                       scale=0.0, scale_col=None, stream=None):
+    """gemm_s8_zp for callers that cannot allocate device memory: the library uses
+    its own fixed scratch (IGC_NOALLOC_SCRATCH_BYTES per GPU) instead of a
+    workspace.  Calls that overlap on the GPU race on that scratch."""
+    import torch
+    M, K, lda = _rows(A, "A", (torch.uint8, torch.int8))
+    N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8))
+    if K2 != K:
+        raise ValueError("A and Bt disagree on K")
+    ldc32 = _rows(C32, "C32", torch.int32)[2] if C32 is not None else 0
+    ldc8 = _rows(C8, "C8", torch.int8)[2] if C8 is not None else 0
+    rc = lib().gemm_s8_zp_noalloc(M, N, K, _ptr(A), 1 if A.dtype == torch.int8 else 0, lda,
+                                  _ptr(Bt), 1 if Bt.dtype == torch.int8 else 0, ldb,
+                                  int(zA), _ptr(zA_row), int(zB), _ptr(zB_col),
+                                  _ptr(C32), ldc32, _ptr(C8), ldc8, float(scale), _ptr(scale_col),
+                                  _stream(stream))
+    _check(rc, "gemm_s8_zp_noalloc")
     return C32, C8
 
 

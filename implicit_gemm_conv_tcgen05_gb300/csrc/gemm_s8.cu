@@ -17,6 +17,8 @@
 //     with zA'_i = zA_i - oA and zB'_j = zB_j - oB -- the zero-point expansion of
 //     sum_k (A'[i,k] - zA'_i)(B'[j,k] - zB'_j) = sum_k (A_q - zA_i)(B_q - zB_j),
 //     then C8 = clamp(rne(fp32(C32) * scale_j), -128, 127).
+#include <mutex>
+
 #include "launch.cuh"
 
 using namespace igc;
@@ -241,4 +243,61 @@ extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_
   }
   return gemm_s8_zp_run(M, N, K, a_signed, b_signed, zA, zA_row, zB, zB_col, C32, ldc32, C8,
                         ldc8, scale, scale_col, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------
+// gemm_s8_zp_noalloc: the same operation for callers that cannot allocate
+// device memory.  Its scratch is a fixed array in the library's device image
+// (every GPU that loads the library holds it until the process exits); the
+// caller still passes inputs and outputs.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(IGC_NOALLOC_SCRATCH_BYTES);
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocSlot {
+  std::once_flag once;
+  void* ptr = nullptr;
+  int rc = IGC_ERR_CUDA;
+};
+NoAllocSlot g_noalloc_slots[64];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IGC_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return IGC_ERR_UNSUPPORTED;
+  NoAllocSlot& s = g_noalloc_slots[dev];
+  std::call_once(s.once, [&] {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess && p != nullptr) {
+      s.ptr = p;
+      s.rc = IGC_OK;
+    } else {
+      s.rc = IGC_ERR_CUDA;
+    }
+  });
+  *out = s.ptr;
+  return s.rc;
+}
+
+}  // namespace
+
+extern "C" int gemm_s8_zp_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,
+                                  int64_t lda, const void* Bt, int b_signed, int64_t ldb,
+                                  int32_t zA, const int32_t* zA_row, int32_t zB,
+                                  const int32_t* zB_col, int32_t* C32, int64_t ldc32, int8_t* C8,
+                                  int64_t ldc8, float scale, const float* scale_col,
+                                  igc_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return IGC_ERR_INVALID_ARG;
+  if (gemm_s8_zp_workspace_size(M, N, K) > kNoAllocScratchBytes) return IGC_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != IGC_OK) return rc;
+  return gemm_s8_zp(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, zA, zA_row, zB, zB_col, C32,
+                    ldc32, C8, ldc8, scale, scale_col, scratch, kNoAllocScratchBytes, stream);
 }

@@ -166,6 +166,41 @@ int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
                    igc_stream_t stream);
 
 /*
+ * gemm_s8_zp_noalloc -- gemm_s8_zp without a caller-provided workspace, for
+ * callers that cannot allocate device memory: for example code running
+ * inside a host framework that owns all device memory through its own pool
+ * and forbids direct cudaMalloc, or a service that must not allocate once it
+ * is serving because an allocation could fail or stall in the middle of a
+ * request.  (The pages have no counterpart of this entry point.)
+ *
+ * Same arguments, results and rounding as gemm_s8_zp, minus the workspace.
+ * Its scratch is a fixed array of IGC_NOALLOC_SCRATCH_BYTES in the library's
+ * device image; every GPU that loads the library holds that memory until the
+ * process exits.  The call allocates nothing (no cudaMalloc, cudaFree or any
+ * allocating library routine); the caller still provides inputs and outputs.
+ *  - Problems whose gemm_s8_zp_workspace_size(M, N, K) exceeds
+ *    IGC_NOALLOC_SCRATCH_BYTES are rejected with IGC_ERR_WORKSPACE before
+ *    anything is enqueued (e.g. 2048^3 fits, 4096^3 does not).
+ *  - The first call on a device looks up the device address of the scratch
+ *    array (cudaGetSymbolAddress, with that device current) and caches it;
+ *    make that first call before any stream capture.
+ *  - Every call shares the one array and leaves its contents behind; each
+ *    call rewrites everything it later reads, so nothing needs clearing.
+ *    Calls that overlap on the GPU (e.g. on two streams at once) race on the
+ *    scratch and give wrong results: serialise them.
+ */
+#define IGC_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int gemm_s8_zp_noalloc(int64_t M, int64_t N, int64_t K,
+                       const void *A, int a_signed, int64_t lda,
+                       const void *Bt, int b_signed, int64_t ldb,
+                       int32_t zA, const int32_t *zA_row,
+                       int32_t zB, const int32_t *zB_col,
+                       int32_t *C32, int64_t ldc32,
+                       int8_t *C8, int64_t ldc8,
+                       float scale, const float *scale_col,
+                       igc_stream_t stream);
+
+/*
  * conv2d_nhwc_f16_implicit -- 2-D convolution (cross-correlation, no kernel
  * flip) as an implicit GEMM ([P3] "准备和算法"): no im2col tensor is built;
  * the A operand is gathered by TMA in im2col mode.
