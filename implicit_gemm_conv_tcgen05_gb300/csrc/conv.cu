@@ -47,19 +47,16 @@ extern "C" int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R
   if (!aligned16(x) || !aligned16(w)) return IGC_ERR_MISALIGNED;
 
   const int Kg = R * S * C;
-  CUtensorMap tmA, tmB;
-  rc = encode_im2col_nhwc(&tmA, x, N, H, W, C, lower_h, lower_w, upper_h, upper_w, BK, BM,
+  CUtensorMap tmA;
+  rc = encode_im2col_nhwc(&tmA, x, N, H, W, C, lower_h, lower_w, upper_h, upper_w, BK, BM_CTA,
                           stride_h, stride_w);
-  if (rc != IGC_OK) return rc;
-  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w, Kg, K,
-                       static_cast<uint64_t>(Kg) * 2, BK, BN);
   if (rc != IGC_OK) return rc;
 
   KParams p{};
   p.M = static_cast<int>(M);
   p.N = K;
   p.K = Kg;
-  p.conv_cblocks = (C + BK - 1) / BK;
+  p.conv_cblocks = (C + KS - 1) / KS;
   p.num_kb = R * S * p.conv_cblocks;
   p.chunk_kb = p.num_kb;
   p.conv_P = static_cast<int>(P);
@@ -76,5 +73,6 @@ extern "C" int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R
   p.out_f32 = y_f32_check;
   p.ldo32 = K;
   p.vec_ok = vec_store_ok(y, K, 2) && vec_store_ok(y_f32_check, K, 4);
-  return launch_tc_gemm<Mode::ConvF16>(dev, tmA, tmB, p, stream);
+  return launch_auto_bn<Mode::ConvF16>(dev, tmA, w, Kg, K, static_cast<uint64_t>(Kg) * 2, p,
+                                       stream);
 }

@@ -31,17 +31,15 @@ extern "C" int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if (!aligned16(A) || !aligned16(Bt) || (lda % 8) != 0 || (ldb % 8) != 0)
     return IGC_ERR_MISALIGNED;
 
-  CUtensorMap tmA, tmB;
-  rc = encode_tiled_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK, BM);
-  if (rc != IGC_OK) return rc;
-  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Bt, K, N, ldb * 2, BK, BN);
+  CUtensorMap tmA;
+  rc = encode_tiled_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, lda * 2, BK, BM_CTA);
   if (rc != IGC_OK) return rc;
 
   KParams p{};
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.num_kb = static_cast<int>((K + BK - 1) / BK);
+  p.num_kb = static_cast<int>((K + KS - 1) / KS);
   p.chunk_kb = p.num_kb;
   p.out = C;
   p.ldo = ldc;
@@ -49,5 +47,5 @@ extern "C" int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   p.out_f32 = C_f32_check;
   p.ldo32 = ldc32;
   p.vec_ok = vec_store_ok(C, ldc, esize) && vec_store_ok(C_f32_check, ldc32, 4);
-  return launch_tc_gemm<Mode::GemmF16>(dev, tmA, tmB, p, stream);
+  return launch_auto_bn<Mode::GemmF16>(dev, tmA, Bt, K, N, ldb * 2, p, stream);
 }

@@ -194,17 +194,16 @@ extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int
 
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   const long long Kp = k_padded(K);
-  CUtensorMap tmA, tmB;
-  rc = encode_tiled_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws + l.a_off, Kp, M, Kp * 2, BK, BM);
-  if (rc != IGC_OK) return rc;
-  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws + l.b_off, Kp, N, Kp * 2, BK, BN);
+  CUtensorMap tmA;
+  rc = encode_tiled_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws + l.a_off, Kp, M, Kp * 2, BK,
+                       BM_CTA);
   if (rc != IGC_OK) return rc;
 
   KParams p{};
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.num_kb = static_cast<int>((Kp + BK - 1) / BK);
+  p.num_kb = static_cast<int>((Kp + KS - 1) / KS);
   p.chunk_kb = kIntChunkKb;
   p.c32 = C32;
   p.ldc32 = ldc32;
@@ -221,7 +220,7 @@ extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int
   p.scale = scale;
   p.scale_col = scale_col;
   p.vec_ok = vec_store_ok(C32, ldc32, 4) && vec_store_ok(C8, ldc8, 1);
-  return launch_tc_gemm<Mode::GemmInt>(dev, tmA, tmB, p, stream);
+  return launch_auto_bn<Mode::GemmInt>(dev, tmA, ws + l.b_off, Kp, N, Kp * 2, p, stream);
 }
 
 extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,

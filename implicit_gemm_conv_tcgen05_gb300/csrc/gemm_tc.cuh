@@ -1,4 +1,4 @@
-// Persistent, warp-specialised tcgen05 GEMM for sm_103a.
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a, 2-CTA (cta_group::2) tiles.
 //
 // One kernel template serves the three operations of the library:
 //   GemmF16 : C[i,j] = sum_k A[i,k] * Bt[j,k], fp16 operands, fp32 accumulate
@@ -15,16 +15,23 @@
 //             requantisation fused into the epilogue (page "TVM在CUDA GPU上跑GEMM
 //             的全套张量化实现", §2.3).
 //
-// Tile 128 x 256 x 64, fp32 accumulators in tensor memory.  Warp roles:
-//   warp 0      TMA producer (one lane): global -> 4-stage shared-memory ring,
-//               128-byte swizzle, completion on `full[s]` mbarriers.
-//   warp 1      MMA issuer (one lane): tcgen05.mma kind::f16 128x256x16, 4 per
-//               k-block; tcgen05.commit frees ring stages (`empty[s]`) and hands
-//               finished accumulators to the epilogue (`tfull[a]`).  Also owns the
-//               tensor-memory allocation (512 columns = two accumulators, so the
-//               epilogue of one tile overlaps the main loop of the next).
-//   warps 2..9  epilogue: tcgen05.ld of their lane quadrant / column half, fused
-//               output math, predicated global stores.
+// A cluster of two CTAs (on two SMs) computes one 256 x BN output tile with
+// tcgen05.mma.cta_group::2 (M = 256): CTA r holds rows [128 r, 128 r + 128) of
+// the A tile and rows [BN/2 r, BN/2 (r+1)) of the B tile in its own shared
+// memory, and receives its 128 x BN accumulator in its own tensor memory.
+// Warp roles in each CTA:
+//   warp 0      TMA producer (one lane): its CTA's halves of A and B into a
+//               multi-stage ring (128-byte swizzle); both CTAs' copies complete
+//               on the leader CTA's `full[s]` barrier.
+//   warp 1      tensor-memory owner; in the leader CTA also the MMA issuer (one
+//               lane): 4 x tcgen05.mma per 64-deep k-block, tcgen05.commit
+//               multicast to both CTAs frees ring stages (`empty[s]`) and hands
+//               finished accumulators to both epilogues (`tfull[a]`).
+//   warps 2..9  epilogue: tcgen05.ld of their lane quadrant / column half,
+//               fused output math, predicated global stores; they release an
+//               accumulator on the leader's `tempty[a]` (16 arrivals).
+// Two accumulators (2 x BN of the 512 TMEM columns) let the epilogue of one
+// tile overlap the main loop of the next.
 //
 // GemmInt keeps each accumulation chunk (chunk_kb k-blocks = 256 k) below
 // 2^22 in magnitude, so fp32 holds it exactly; the epilogue drains every chunk
@@ -39,19 +46,34 @@ namespace igc {
 
 enum class Mode : int { GemmF16 = 0, ConvF16 = 1, GemmInt = 2 };
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // 64 fp16 = one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr int BM = 256;        // rows per cluster tile (128 per CTA)
+constexpr int BM_CTA = 128;
+constexpr int BK = 64;         // 64 fp16 = one 128-byte swizzle row (one TMA box, one atom)
+constexpr int kAtoms = 2;      // swizzle atoms along k per pipeline stage
+constexpr int KS = BK * kAtoms;  // k depth of one pipeline stage (8 MMAs of k = 16)
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
-constexpr uint32_t kTmemCols = 2 * BN;         // two 128 x 256 fp32 accumulators
-constexpr uint32_t kStageABytes = BM * BK * 2;
-constexpr uint32_t kStageBBytes = BN * BK * 2;
-constexpr uint32_t kBarrierBytes = 256;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
-                              kStages * (kStageABytes + kStageBBytes) + kBarrierBytes;
-constexpr int kIntChunkKb = 4;  // 256 k per exact fp32 chunk
+constexpr uint32_t kAtomABytes = BM_CTA * BK * 2;   // 16 KB
+constexpr uint32_t kStageABytes = kAtomABytes * kAtoms;
+constexpr uint32_t kBarrierBytes = 512;
+constexpr size_t kSmemBudget = 227 * 1024;
+constexpr int kIntChunkKb = 256 / KS;  // stages per exact fp32 chunk (256 k)
+
+template <int BN>
+struct TileCfg {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+  static constexpr int kBNHalf = BN / 2;                        // B rows per CTA
+  static constexpr uint32_t kAtomBBytes = kBNHalf * BK * 2;
+  static constexpr uint32_t kStageBBytes = kAtomBBytes * kAtoms;
+  static constexpr uint32_t kStageBytes = kStageABytes + kStageBBytes;
+  static constexpr int kStages =
+      static_cast<int>((kSmemBudget - 1024 - kBarrierBytes) / kStageBytes) > 8
+          ? 8
+          : static_cast<int>((kSmemBudget - 1024 - kBarrierBytes) / kStageBytes);
+  static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes;
+  static constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256 : 512;  // power of two >= 2*BN
+  static constexpr int kEpiCols = BN / 2;  // columns per epilogue warp
+};
 
 // wait sites, reported in the device status word
 enum : uint32_t {
@@ -60,40 +82,36 @@ enum : uint32_t {
   kSiteMmaFull = 3,
   kSiteEpiFull = 4,
   kSiteDrain = 5,
+  kSiteTmemMismatch = 6,
 };
 
 struct KParams {
-  // GEMM view of the problem
   int M, N, K;
   int num_kb;
   int tiles_m, tiles_n, num_tiles;
-  int group_m;   // tile raster: this many m-blocks are walked together
-  int chunk_kb;  // k-blocks per accumulation chunk (>= num_kb except GemmInt)
-  // convolution geometry (ConvF16)
+  int group_m;
+  int chunk_kb;
   int conv_P, conv_Q, conv_cblocks, conv_S, conv_C;
   int pad_h, pad_w, stride_h, stride_w;
-  // floating outputs (GemmF16 / ConvF16)
   void* out;
   long long ldo;
-  int out_f16;  // 1: out is fp16 (RNE), 0: out is fp32
+  int out_f16;
   float* out_f32;
   long long ldo32;
-  int vec_ok;  // outputs allow 16-byte vector stores
-  // integer outputs (GemmInt)
+  int vec_ok;
   int32_t* c32;
   long long ldc32;
   int8_t* c8;
   long long ldc8;
-  const int32_t* rsumA;  // sum_k A'[i,k] of the shifted operand
-  const int32_t* csumB;  // sum_k B'[j,k]
+  const int32_t* rsumA;
+  const int32_t* csumB;
   int32_t zA;
   const int32_t* zA_row;
   int32_t zB;
   const int32_t* zB_col;
-  int32_t oA, oB;  // shift applied by the pre-pass: A' = A_q - oA, B' = B_q - oB
+  int32_t oA, oB;
   float scale;
   const float* scale_col;
-  // control
   unsigned long long wait_limit_ns;
   unsigned long long* status;
 };
@@ -109,24 +127,24 @@ __device__ __forceinline__ void tile_coords(const KParams& p, int t, int& mb, in
 }
 
 // ---------------------------------------------------------------------------
-// epilogue helpers
+// epilogue helpers (one thread = one output row, NC consecutive columns)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bits) {
   __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Row m of the tile, columns n0 .. n0+127, values v (fp32 bit patterns).
+template <int NC>
 __device__ __forceinline__ void store_row_float(const KParams& p, int m, int n0,
-                                                const uint32_t (&v)[128]) {
+                                                const uint32_t (&v)[NC]) {
   if (m >= p.M) return;
-  const bool full = p.vec_ok && (n0 + 128 <= p.N);
+  const bool full = p.vec_ok && (n0 + NC <= p.N);
   if (p.out != nullptr) {
     if (p.out_f16) {
       __half* row = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(m) * p.ldo + n0;
       if (full) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < NC / 8; ++j) {
           uint4 q;
           q.x = pack_half2(v[8 * j + 0], v[8 * j + 1]);
           q.y = pack_half2(v[8 * j + 2], v[8 * j + 3]);
@@ -136,19 +154,19 @@ __device__ __forceinline__ void store_row_float(const KParams& p, int m, int n0,
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < NC; ++i)
           if (n0 + i < p.N) row[i] = __float2half_rn(__uint_as_float(v[i]));
       }
     } else {
       float* row = reinterpret_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo + n0;
       if (full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < NC / 4; ++j)
           reinterpret_cast<uint4*>(row)[j] =
               make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < NC; ++i)
           if (n0 + i < p.N) row[i] = __uint_as_float(v[i]);
       }
     }
@@ -157,12 +175,12 @@ __device__ __forceinline__ void store_row_float(const KParams& p, int m, int n0,
     float* row = p.out_f32 + static_cast<size_t>(m) * p.ldo32 + n0;
     if (full) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < NC / 4; ++j)
         reinterpret_cast<uint4*>(row)[j] =
             make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 128; ++i)
+      for (int i = 0; i < NC; ++i)
         if (n0 + i < p.N) row[i] = __uint_as_float(v[i]);
     }
   }
@@ -177,27 +195,28 @@ __device__ __forceinline__ int8_t requant_i8(int32_t c, float s) {
 }
 
 // sum[] holds, per column, n_chunks * 0x4B400000 + sum_k A'B' (mod 2^32).
+template <int NC>
 __device__ __forceinline__ void store_row_int(const KParams& p, int m, int n0,
-                                              const uint32_t (&sum)[128], int n_chunks) {
+                                              const uint32_t (&sum)[NC], int n_chunks) {
   if (m >= p.M) return;
   const uint32_t bias = static_cast<uint32_t>(n_chunks) * 0x4B400000u;
   const uint32_t rA = static_cast<uint32_t>(p.rsumA[m]);
   const uint32_t zAp = static_cast<uint32_t>((p.zA_row ? __ldg(p.zA_row + m) : p.zA) - p.oA);
   const uint32_t Ku = static_cast<uint32_t>(p.K);
-  const bool full = p.vec_ok && (n0 + 128 <= p.N);
+  const bool full = p.vec_ok && (n0 + NC <= p.N);
   int32_t* row32 = p.c32 ? p.c32 + static_cast<size_t>(m) * p.ldc32 + n0 : nullptr;
   int8_t* row8 = p.c8 ? p.c8 + static_cast<size_t>(m) * p.ldc8 + n0 : nullptr;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {  // 16 columns per step
+  for (int j = 0; j < NC / 16; ++j) {
     int32_t c[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int col = j * 16 + i;
-      const int n = n0 + col;
+      const int n = n0 + j * 16 + i;
       const int nn = n < p.N ? n : p.N - 1;  // keep the side loads in bounds on the tail
-      const uint32_t zBp = static_cast<uint32_t>((p.zB_col ? __ldg(p.zB_col + nn) : p.zB) - p.oB);
+      const uint32_t zBp =
+          static_cast<uint32_t>((p.zB_col ? __ldg(p.zB_col + nn) : p.zB) - p.oB);
       const uint32_t cB = static_cast<uint32_t>(__ldg(p.csumB + nn));
-      const uint32_t v = sum[col] - bias - zBp * rA - zAp * cB + Ku * zAp * zBp;
+      const uint32_t v = sum[j * 16 + i] - bias - zBp * rA - zAp * cB + Ku * zAp * zBp;
       c[i] = static_cast<int32_t>(v);
     }
     if (row32) {
@@ -213,58 +232,105 @@ __device__ __forceinline__ void store_row_int(const KParams& p, int m, int n0,
       }
     }
     if (row8) {
-      int8_t q[16];
+      uint32_t w[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int n = n0 + j * 16 + i;
-        const int nn = n < p.N ? n : p.N - 1;
-        const float s = p.scale_col ? __ldg(p.scale_col + nn) : p.scale;
-        q[i] = requant_i8(c[i], s);
+      for (int i = 0; i < 4; ++i) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int n = n0 + j * 16 + 4 * i + b;
+          const int nn = n < p.N ? n : p.N - 1;
+          const float s = p.scale_col ? __ldg(p.scale_col + nn) : p.scale;
+          packed |= static_cast<uint32_t>(static_cast<uint8_t>(requant_i8(c[4 * i + b], s)))
+                    << (8 * b);
+        }
+        w[i] = packed;
       }
       if (full) {
-        uint4 w;
-        w.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
-              ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
-        w.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) |
-              ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
-        w.z = (uint32_t)(uint8_t)q[8] | ((uint32_t)(uint8_t)q[9] << 8) |
-              ((uint32_t)(uint8_t)q[10] << 16) | ((uint32_t)(uint8_t)q[11] << 24);
-        w.w = (uint32_t)(uint8_t)q[12] | ((uint32_t)(uint8_t)q[13] << 8) |
-              ((uint32_t)(uint8_t)q[14] << 16) | ((uint32_t)(uint8_t)q[15] << 24);
-        reinterpret_cast<uint4*>(row8)[j] = w;
+        reinterpret_cast<uint4*>(row8)[j] = make_uint4(w[0], w[1], w[2], w[3]);
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (n0 + j * 16 + i < p.N) row8[j * 16 + i] = q[i];
+          if (n0 + j * 16 + i < p.N)
+            row8[j * 16 + i] = static_cast<int8_t>((w[i / 4] >> (8 * (i % 4))) & 0xFFu);
       }
     }
+  }
+}
+
+// Loads NC consecutive TMEM columns (this warp's 32 lanes) into v: 32 columns
+// per tcgen05.ld, then 16 for a remainder.  The caller waits (tmem_ld_wait).
+template <int NC>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&v)[NC]) {
+#pragma unroll
+  for (int j = 0; j < NC / 32; ++j) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + j * 32, r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[j * 32 + i] = r[i];
+  }
+  if constexpr (NC % 32 != 0) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr + (NC / 32) * 32, r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[(NC / 32) * 32 + i] = r[i];
+  }
+}
+
+// Adds the exact integers held in NC fp32 TMEM columns to the running sums
+// (bits of x + 1.5*2^23, i.e. 0x4B400000 + x for |x| <= 2^22): 32 columns per load.
+template <int NC>
+__device__ __forceinline__ void tmem_drain_add(uint32_t taddr, uint32_t (&sum)[NC]) {
+#pragma unroll
+  for (int j = 0; j < NC / 32; ++j) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + j * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      sum[j * 32 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r[i]), 12582912.0f));
+  }
+  if constexpr (NC % 32 != 0) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr + (NC / 32) * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      sum[(NC / 32) * 32 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r[i]), 12582912.0f));
   }
 }
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <Mode kMode>
+template <Mode kMode, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     igc_tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using Cfg = TileCfg<BN>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int NC = Cfg::kEpiCols;
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
 
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kStageBBytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = tfull + 2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * Cfg::kStageBBytes);
+  uint64_t* full = bars;                 // leader: both CTAs' copies of stage s landed
+  uint64_t* empty = bars + kStages;      // each CTA: stage s may be overwritten
+  uint64_t* tfull = bars + 2 * kStages;  // each CTA: accumulator a is ready
+  uint64_t* tempty = tfull + 2;          // leader: both epilogues released accumulator a
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
   const int lane = static_cast<int>(lane_id());
+  const uint32_t rank = cluster_ctarank();  // 0 = leader
+  const int cluster = static_cast<int>(blockIdx.x) >> 1;
+  const int num_clusters = static_cast<int>(gridDim.x) >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -273,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps);
+      mbar_init(&tempty[a], 2 * kEpiWarps);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -284,64 +350,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_2cta(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish_2cta();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
+  // The pair's MMAs write both CTAs' tensor memory at the leader's address: both
+  // allocations must agree, else the pair does no work at all.
+  const uint32_t peer_base = ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), rank ^ 1u));
+  const bool pair_ok = peer_base == tmem_base;
+  if (!pair_ok && threadIdx.x == 0) report_status(p.status, kStatusBadLaunch, kSiteTmemMismatch);
+  // the leader's barriers, as cluster addresses usable from either CTA
+  const uint32_t full_lead = mapa_shared(smem_u32(full), 0);
+  const uint32_t tempty_lead = mapa_shared(smem_u32(tempty), 0);
 
-  if (warp == 0) {
+  if (!pair_ok) {
+    // nothing: go straight to the teardown
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
-        int cn = 0, ch = 0, cw = 0;
-        if constexpr (kMode == Mode::ConvF16) {
-          const int m0 = mb * BM;
-          const int PQ = p.conv_P * p.conv_Q;
-          cn = m0 / PQ;
-          const int rem = m0 - cn * PQ;
-          const int pp = rem / p.conv_Q;
-          const int qq = rem - pp * p.conv_Q;
-          ch = pp * p.stride_h - p.pad_h;
-          cw = qq * p.stride_w - p.pad_w;
-        }
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, lim, abort_flag, p.status, kSiteProducerEmpty))
-            goto producer_done;
+    // The whole warp runs the loop (converged); lane 0 issues the copies.
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    for (int t = cluster; t < p.num_tiles; t += num_clusters) {
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int m_cta = mb * BM + static_cast<int>(rank) * BM_CTA;
+      const int n_cta = nb * BN + static_cast<int>(rank) * Cfg::kBNHalf;
+      int cn = 0, ch = 0, cw = 0;
+      if constexpr (kMode == Mode::ConvF16) {
+        const int PQ = p.conv_P * p.conv_Q;
+        cn = m_cta / PQ;
+        const int rem = m_cta - cn * PQ;
+        const int pp = rem / p.conv_Q;
+        const int qq = rem - pp * p.conv_Q;
+        ch = pp * p.stride_h - p.pad_h;
+        cw = qq * p.stride_w - p.pad_w;
+      }
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, lim, abort_flag,
+                                                p.status, kSiteProducerEmpty)))
+          goto producer_done;
+        if (lane == 0) {
           uint8_t* a_dst = sA + stage * kStageABytes;
-          uint8_t* b_dst = sB + stage * kStageBBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageABytes + kStageBBytes);
+          uint8_t* b_dst = sB + stage * Cfg::kStageBBytes;
+          const uint32_t bar = full_lead + static_cast<uint32_t>(stage) * 8u;
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * Cfg::kStageBytes);
           if constexpr (kMode == Mode::ConvF16) {
             const int tap = kb / p.conv_cblocks;
-            const int c0 = (kb - tap * p.conv_cblocks) * BK;
+            const int c0 = (kb - tap * p.conv_cblocks) * KS;
             const int r = tap / p.conv_S;
             const int s = tap - r * p.conv_S;
-            tma_load_im2col_4d(a_dst, &tmA, &full[stage], c0, cw, ch, cn,
-                               static_cast<uint16_t>(s), static_cast<uint16_t>(r));
-            tma_load_2d(b_dst, &tmB, &full[stage], tap * p.conv_C + c0, nb * BN);
+#pragma unroll
+            for (int j = 0; j < kAtoms; ++j) {
+              tma_load_im2col_4d_2cta(a_dst + j * kAtomABytes, &tmA, bar, c0 + j * BK, cw, ch, cn,
+                                      static_cast<uint16_t>(s), static_cast<uint16_t>(r));
+              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, &tmB, bar,
+                               tap * p.conv_C + c0 + j * BK, n_cta);
+            }
           } else {
-            tma_load_2d(a_dst, &tmA, &full[stage], kb * BK, mb * BM);
-            tma_load_2d(b_dst, &tmB, &full[stage], kb * BK, nb * BN);
-          }
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+#pragma unroll
+            for (int j = 0; j < kAtoms; ++j) {
+              tma_load_2d_2cta(a_dst + j * kAtomABytes, &tmA, bar, kb * KS + j * BK, m_cta);
+              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, &tmB, bar, kb * KS + j * BK, n_cta);
+            }
           }
         }
+        __syncwarp();
+        ++issued;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-    producer_done:
-      // Make sure no copy into this CTA's shared memory is still in flight
-      // before the CTA can exit (only matters when a wait gave up).
-      if (*abort_flag) {
+    }
+  producer_done:
+    if (lane == 0 && *abort_flag && issued > 0) {
+      // The copies signal the leader's barriers; give this CTA's own in-flight
+      // copies time to land before the CTA may exit (a copy takes microseconds).
+      if (rank == 0) {
         int s = stage;
         uint32_t ph = phase;
         for (long long i = 0; i < issued && i < kStages; ++i) {
@@ -350,47 +440,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             ph ^= 1u;
           }
           int dummy = 0;
-          mbar_wait(&full[s], ph, lim, &dummy, nullptr, kSiteDrain);
+          mbar_wait(&full[s], ph, lim / 64 + 1000, &dummy, nullptr, kSiteDrain);
+        }
+      } else {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    // The whole warp runs the loop (converged); lane 0 issues MMAs and commits.
+    if (rank == 0) {
       constexpr uint32_t idesc = make_idesc_f16_f32(BM, BN);
+      // descriptors of stage 0, atom 0, k 0; the start-address field (bits 0-13,
+      // in 16-byte units) is advanced by adding offsets >> 4 (no carry: < 256 KB)
+      const uint64_t adesc0 = make_sw128_kmajor_desc(smem_u32(sA));
+      const uint64_t bdesc0 = make_sw128_kmajor_desc(smem_u32(sB));
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      for (int t = cluster; t < p.num_tiles; t += num_clusters) {
+        int kin = 0;
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          const int kin = kb % p.chunk_kb;
           if (kin == 0) {
-            if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, lim, abort_flag, p.status,
-                           kSiteMmaTmemEmpty))
+            if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, lim, abort_flag,
+                                                    p.status, kSiteMmaTmemEmpty)))
               goto mma_done_label;
             tc_fence_after();
           }
-          if (!mbar_wait(&full[stage], phase, lim, abort_flag, p.status, kSiteMmaFull))
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, lim, abort_flag, p.status,
+                                                  kSiteMmaFull)))
             goto mma_done_label;
           tc_fence_after();
-          {
-            const uint32_t a_base = smem_u32(sA + stage * kStageABytes);
-            const uint32_t b_base = smem_u32(sB + stage * kStageBBytes);
+          const bool chunk_end = (kin == p.chunk_kb - 1) || (kb == p.num_kb - 1);
+          if (lane == 0) {
+            const uint64_t a_st = adesc0 + ((static_cast<uint32_t>(stage) * kStageABytes) >> 4);
+            const uint64_t b_st = bdesc0 + ((static_cast<uint32_t>(stage) * Cfg::kStageBBytes) >> 4);
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              const uint64_t ad = make_sw128_kmajor_desc(a_base + k * 32);
-              const uint64_t bd = make_sw128_kmajor_desc(b_base + k * 32);
-              umma_f16_ss(d_tmem, ad, bd, idesc, (kin > 0 || k > 0) ? 1u : 0u);
+            for (int j = 0; j < kAtoms; ++j) {
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                const uint64_t ad = a_st + ((j * kAtomABytes + k * 32) >> 4);
+                const uint64_t bd = b_st + ((j * Cfg::kAtomBBytes + k * 32) >> 4);
+                umma_f16_ss_2cta(d_tmem, ad, bd, idesc, (kin > 0 || j > 0 || k > 0) ? 1u : 0u);
+              }
             }
+            umma_commit_2cta_multicast(&empty[stage], 0x3);
+            if (chunk_end) umma_commit_2cta_multicast(&tfull[acc], 0x3);
           }
-          umma_commit(&empty[stage]);
-          if (kin == p.chunk_kb - 1 || kb == p.num_kb - 1) {
-            umma_commit(&tfull[acc]);
+          __syncwarp();
+          if (chunk_end) {
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
           }
+          if (++kin == p.chunk_kb) kin = 0;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -398,96 +504,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     mma_done_label:
-      // every MMA issued by this thread has finished once mma_done completes
-      umma_commit(mma_done);
-      {
+      if (lane == 0) {
+        // every MMA issued by this thread has finished once mma_done completes
+        umma_commit_2cta(mma_done);
         int dummy = 0;
         mbar_wait(mma_done, 0, lim, &dummy, p.status, kSiteDrain);
       }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;
     const int quad = warp & 3;  // tcgen05.ld: warp w may access lanes 32*(w%4) .. +31
-    const int half = ew >> 2;   // which 128-column half of the tile
-    const int row_in_tile = quad * 32 + lane;
+    const int half = ew >> 2;   // which column half of the tile
+    const int row_in_cta = quad * 32 + lane;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(half * 128);
+                               static_cast<uint32_t>(half * NC);
     const int n_chunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    for (int t = cluster; t < p.num_tiles; t += num_clusters) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
-      const int m = mb * BM + row_in_tile;
-      const int n0 = nb * BN + half * 128;
+      const int m = mb * BM + static_cast<int>(rank) * BM_CTA + row_in_cta;
+      const int n0 = nb * BN + half * NC;
       if constexpr (kMode != Mode::GemmInt) {
-        // every lane waits (acquire); the warp then agrees before the .aligned loads
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&tfull[acc], acc_phase, lim, abort_flag, p.status, kSiteEpiFull)))
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag,
+                                                        p.status, kSiteEpiFull)))
           goto epi_done;
         tc_fence_after();
-        uint32_t v[128];
-        {
-          const uint32_t a = lane_base + static_cast<uint32_t>(acc * BN);
-          uint32_t r0[32], r1[32], r2[32], r3[32];
-          tmem_ld_32x32b_x32(a + 0, r0);
-          tmem_ld_32x32b_x32(a + 32, r1);
-          tmem_ld_32x32b_x32(a + 64, r2);
-          tmem_ld_32x32b_x32(a + 96, r3);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[i] = r0[i];
-            v[32 + i] = r1[i];
-            v[64 + i] = r2[i];
-            v[96 + i] = r3[i];
-          }
-        }
+        uint32_t v[NC];
+        tmem_load_cols<NC>(lane_base + static_cast<uint32_t>(acc * BN), v);
+        tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
-        store_row_float(p, m, n0, v);
+        store_row_float<NC>(p, m, n0, v);
       } else {
-        uint32_t sum[128];
+        uint32_t sum[NC];
 #pragma unroll
-        for (int i = 0; i < 128; ++i) sum[i] = 0u;
+        for (int i = 0; i < NC; ++i) sum[i] = 0u;
         for (int c = 0; c < n_chunks; ++c) {
           if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag,
-                                                  p.status, kSiteEpiFull)))
+                                                          p.status, kSiteEpiFull)))
             goto epi_done;
           tc_fence_after();
-          const uint32_t a = lane_base + static_cast<uint32_t>(acc * BN);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(a + j * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              sum[j * 32 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r[i]), 12582912.0f));
-          }
+          tmem_drain_add<NC>(lane_base + static_cast<uint32_t>(acc * BN), sum);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[acc]);
+          if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
-        store_row_int(p, m, n0, sum, n_chunks);
+        store_row_int<NC>(p, m, n0, sum, n_chunks);
       }
     }
   epi_done:;
   }
 
   // ---------------------------------------------------------------- teardown
+  // No CTA of the pair may exit (or free tensor memory) while its peer can still
+  // touch its shared memory or barriers.
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_2cta(tmem_base, Cfg::kTmemCols);
   }
 }
 

@@ -1,4 +1,6 @@
-// Shared launch code for the tcgen05 GEMM kernel template.
+// Shared launch code for the tcgen05 GEMM kernel template: cluster launch of
+// CTA pairs, grid sized to the pairs that fit at once, tile width chosen per
+// problem to balance the last wave.
 #pragma once
 
 #include <mutex>
@@ -8,22 +10,68 @@
 
 namespace igc {
 
-template <Mode kMode>
+template <Mode kMode, int BN>
+struct KernelSlot {
+  std::once_flag once[64];
+  int rc[64];
+  int max_clusters[64];
+};
+
+template <Mode kMode, int BN>
+KernelSlot<kMode, BN>& kernel_slot() {
+  static KernelSlot<kMode, BN> s;
+  return s;
+}
+
+// Sets the kernel's shared-memory attribute and finds how many CTA pairs fit
+// on the device at once (cached per device).
+template <Mode kMode, int BN>
+int kernel_setup(const DeviceInfo& dev, int* max_clusters) {
+  auto& s = kernel_slot<kMode, BN>();
+  const int d = dev.device;
+  std::call_once(s.once[d], [&] {
+    s.rc[d] = IGC_ERR_CUDA;
+    s.max_clusters[d] = 0;
+    if (dev.smem_optin < TileCfg<BN>::kSmemBytes) {
+      s.rc[d] = IGC_ERR_UNSUPPORTED;
+      return;
+    }
+    auto kern = igc_tc_gemm_kernel<kMode, BN>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(TileCfg<BN>::kSmemBytes)) != cudaSuccess)
+      return;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+        cudaSuccess)
+      (void)cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = dev.sm_count / 2;  // one CTA per SM, pairs
+    }
+    s.max_clusters[d] = n;
+    s.rc[d] = IGC_OK;
+  });
+  *max_clusters = s.max_clusters[d];
+  return s.rc[d];
+}
+
+template <Mode kMode, int BN>
 int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                    KParams p, cudaStream_t stream) {
-  static std::once_flag attr_once[64];
-  static int attr_rc[64];
-  const int d = dev.device;
-  std::call_once(attr_once[d], [&] {
-    attr_rc[d] = cudaFuncSetAttribute(igc_tc_gemm_kernel<kMode>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kSmemBytes)) == cudaSuccess
-                     ? IGC_OK
-                     : IGC_ERR_CUDA;
-  });
-  if (attr_rc[d] != IGC_OK) return attr_rc[d];
-  if (dev.smem_optin < kSmemBytes) return IGC_ERR_UNSUPPORTED;
-
+  int max_clusters = 0;
+  int rc = kernel_setup<kMode, BN>(dev, &max_clusters);
+  if (rc != IGC_OK) return rc;
   p.tiles_m = static_cast<int>((static_cast<long long>(p.M) + BM - 1) / BM);
   p.tiles_n = static_cast<int>((static_cast<long long>(p.N) + BN - 1) / BN);
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
@@ -32,9 +80,72 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   p.group_m = p.tiles_m < 16 ? p.tiles_m : 16;
   p.wait_limit_ns = wait_limit_ns();
   p.status = status_word();
-  const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
-  igc_tc_gemm_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, p);
-  return cudaGetLastError() == cudaSuccess ? IGC_OK : IGC_ERR_CUDA;
+  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN>, tmA, tmB, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return IGC_ERR_CUDA;
+  }
+  return IGC_OK;
+}
+
+// Tile width for an M x N output: the candidate with the smallest estimated
+// time, (waves of tiles over the CTA pairs) x (tile width / relative efficiency
+// of that width); ties go to the wider tile.
+inline int pick_bn(long long M, long long N, int clusters, const int* cands, const double* eff,
+                   int n_cands) {
+  const long long tm = (M + BM - 1) / BM;
+  int best = cands[0];
+  double best_cost = 1e300;
+  for (int i = 0; i < n_cands; ++i) {
+    const long long tiles = tm * ((N + cands[i] - 1) / cands[i]);
+    const long long waves = (tiles + clusters - 1) / clusters;
+    const double cost = static_cast<double>(waves) * cands[i] / eff[i];
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = cands[i];
+    }
+  }
+  return best;
+}
+
+// Tile widths each operation is built for, with their relative mainloop
+// efficiency (wider tiles move fewer operand bytes per flop).
+constexpr int kBnCands[] = {256, 128};
+constexpr double kBnEff[] = {1.0, 0.87};  // measured: fp16 8192^3 at BN 128 runs 0.87x BN 256
+constexpr int kNumBn = sizeof(kBnCands) / sizeof(kBnCands[0]);
+
+// Picks the tile width for this problem, encodes B's tensor map with a box of
+// BN/2 rows (each CTA of the pair loads half of the B tile) and launches.
+template <Mode kMode>
+int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_base,
+                   uint64_t b_inner, uint64_t b_rows, uint64_t b_row_bytes, KParams p,
+                   cudaStream_t stream) {
+  int clusters = 0;
+  int rc = kernel_setup<kMode, kBnCands[0]>(dev, &clusters);
+  if (rc != IGC_OK) return rc;
+  const int bn = pick_bn(p.M, p.N, clusters, kBnCands, kBnEff, kNumBn);
+  CUtensorMap tmB;
+  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b_base, b_inner, b_rows,
+                       b_row_bytes, BK, static_cast<uint32_t>(bn / 2));
+  if (rc != IGC_OK) return rc;
+  switch (bn) {
+    case 256: return launch_tc_gemm<kMode, 256>(dev, tmA, tmB, p, stream);
+    case 128: return launch_tc_gemm<kMode, 128>(dev, tmA, tmB, p, stream);
+    default: return IGC_ERR_UNSUPPORTED;
+  }
 }
 
 // Zero an M x N row-major output (K == 0 case: an empty sum is 0).
