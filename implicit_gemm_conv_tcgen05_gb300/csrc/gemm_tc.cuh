@@ -52,7 +52,16 @@ constexpr int BK = 64;         // 64 fp16 = one 128-byte swizzle row (one TMA bo
 constexpr int kAtoms = 2;      // swizzle atoms along k per pipeline stage
 constexpr int KS = BK * kAtoms;  // k depth of one pipeline stage (8 MMAs of k = 16)
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // 320
+// Three warpgroups: warps 0-3 (TMA producer, MMA issuer / TMEM owner, two idle)
+// and two epilogue warpgroups (warps 4-11).  After set-up the first warpgroup
+// gives registers to the epilogue ones (setmaxnreg): kRegsLow + 2 kRegsHigh
+// warpgroup shares = 56 * 128 + 200 * 256 = 58368 registers, which fits the
+// launch's 384 threads x kMinLaunchRegs (checked on the host before launch).
+constexpr int kThreads = 128 + 32 * kEpiWarps;  // 384
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 200;
+constexpr int kMinLaunchRegs = 152;
+static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kThreads * kMinLaunchRegs, "register split");
 constexpr uint32_t kAtomABytes = BM_CTA * BK * 2;   // 16 KB
 constexpr uint32_t kStageABytes = kAtomABytes * kAtoms;
 constexpr uint32_t kBarrierBytes = 512;
@@ -367,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t full_lead = mapa_shared(smem_u32(full), 0);
   const uint32_t tempty_lead = mapa_shared(smem_u32(tempty), 0);
 
-  if (!pair_ok) {
-    // nothing: go straight to the teardown
-  } else if (warp == 0) {
+  if (warp < 4) {
+    warpgroup_regs_dec<kRegsLow>();
+    if (pair_ok && warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop (converged); lane 0 issues the copies.
     int stage = 0;
@@ -448,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
+    } else if (pair_ok && warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
     // The whole warp runs the loop (converged); lane 0 issues MMAs and commits.
     if (rank == 0) {
@@ -512,9 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+    }
   } else {
+    warpgroup_regs_inc<kRegsHigh>();
+    if (pair_ok) {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
+    const int ew = warp - 4;
     const int quad = warp & 3;  // tcgen05.ld: warp w may access lanes 32*(w%4) .. +31
     const int half = ew >> 2;   // which column half of the tile
     const int row_in_cta = quad * 32 + lane;
@@ -562,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   epi_done:;
+    }
   }
 
   // ---------------------------------------------------------------- teardown

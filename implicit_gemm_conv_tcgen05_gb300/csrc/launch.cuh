@@ -40,9 +40,13 @@ int kernel_setup(const DeviceInfo& dev, int* max_clusters) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(TileCfg<BN>::kSmemBytes)) != cudaSuccess)
       return;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
-        cudaSuccess)
-      (void)cudaGetLastError();
+    // the kernel's register split assumes at least kMinLaunchRegs per thread at launch
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return;
+    if (fa.numRegs < kMinLaunchRegs) {
+      s.rc[d] = IGC_ERR_UNSUPPORTED;
+      return;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);

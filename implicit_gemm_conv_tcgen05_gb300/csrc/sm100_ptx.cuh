@@ -219,6 +219,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+// Per-warpgroup register budget (all warps of a warpgroup execute it).  An
+// increase waits until enough registers are free in the CTA's pool, so the
+// shares of all warpgroups must fit what the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void warpgroup_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void warpgroup_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------------------
 // clusters of two CTAs (cta_group::2)
 // ---------------------------------------------------------------------------
