@@ -164,7 +164,7 @@ class Step:
         self.C8 = torch.empty((8192, 8192), dtype=torch.int8, device=device)
         self.ws = torch.empty(igc.gemm_s8_zp_workspace_size(8192, 8192, 8192), dtype=torch.uint8,
                               device=device)
-        self.launches_per_step = 5  # gemm_f16, conv, 2 x int8 pre-pass, int8 GEMM
+        self.launches_per_step = 4  # gemm_f16, conv, int8 pre-pass (both operands), int8 GEMM
 
     def run(self, ev=None):
         igc = self.igc

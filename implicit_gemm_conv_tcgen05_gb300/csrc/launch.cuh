@@ -81,7 +81,7 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffLL) return IGC_ERR_UNSUPPORTED;
   p.num_tiles = static_cast<int>(tiles);
-  p.group_m = p.tiles_m < 16 ? p.tiles_m : 16;
+  p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;  // m-tiles walked together (measured best of 2-16)
   p.wait_limit_ns = wait_limit_ns();
   p.status = status_word();
   const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
