@@ -230,6 +230,19 @@ def traffic_for(kernel_key: str):
     return float(e["dram_bytes_per_launch"])
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    on_gpu = dist.get_backend() == "nccl"
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if on_gpu else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     torch.cuda.set_device(local_rank)
@@ -270,12 +283,7 @@ def run_ours(args, rank, world, local_rank):
 
     seg = np.array([[ev[j].elapsed_time(ev[j + 1]) for j in range(4)] for ev in evs])  # ms
     step_ms = seg.sum(axis=1)
-    ms_local = float(step_ms.mean())
-    ms = ms_local
-    if world > 1:
-        tt = torch.tensor([ms_local], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(float(step_ms.mean()), world, device)
     value = world * OPS_PER_STEP / (ms * 1e-3) / 1e12
 
     peak_burst, peak_sust, hbm, peak_kind = measured_peaks()
@@ -312,11 +320,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, 20))
         e_ms, h2d, d2h = e2e_measure(step, w3, w4, w5, e2e_steps)
-        e_local = e_ms
-        if world > 1:
-            tt = torch.tensor([e_local], dtype=torch.float64, device=device)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(e_ms, world, device)
         result["e2e"] = {"value": world * OPS_PER_STEP / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                          "ms_per_step": e_ms, "steps": e2e_steps,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
