@@ -29,6 +29,7 @@ IGC_ERR_DEVICE_TIMEOUT = 5
 IGC_ERR_WORKSPACE = 6
 IGC_F32 = 0
 IGC_F16 = 1
+IGC_BF16 = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +59,8 @@ def lib() -> ctypes.CDLL:
             i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
             L.gemm_f16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp]
             L.gemm_f16.restype = i32
+            L.gemm_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp]
+            L.gemm_bf16.restype = i32
             L.gemm_s8_zp.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64,
                                      ctypes.c_int32, vp, ctypes.c_int32, vp,
                                      vp, i64, vp, i64, ctypes.c_float, vp, vp, sz, vp]
@@ -68,6 +71,10 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_int32, vp, vp, i64, vp, i64, ctypes.c_float,
                                          vp, vp, sz, vp]
             L.gemm_s8_zp_run.restype = i32
+            L.gemm_s8_zp_dequant.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64,
+                                             ctypes.c_int32, vp, ctypes.c_int32, vp,
+                                             vp, vp, vp, vp, i64, vp, sz, vp]
+            L.gemm_s8_zp_dequant.restype = i32
             L.gemm_s8_zp_noalloc.argtypes = [i64, i64, i64, vp, i32, i64, vp, i32, i64,
                                              ctypes.c_int32, vp, ctypes.c_int32, vp,
                                              vp, i64, vp, i64, ctypes.c_float, vp, vp]
@@ -191,6 +198,33 @@ def gemm_f16(A, Bt, C=None, C_f32_check=None, stream=None):
     return C
 
 
+def gemm_bf16(A, Bt, C=None, C_f32_check=None, stream=None):
+    """C[i,j] = sum_k A[i,k] Bt[j,k]; A (M,K) bf16, Bt (N,K) bf16 (B column-major),
+    C (M,N) bf16 or fp32, C_f32_check optional fp32 (M,N).  Returns C."""
+    import torch
+    M, K, lda = _rows(A, "A", torch.bfloat16)
+    N, K2, ldb = _rows(Bt, "Bt", torch.bfloat16)
+    if K2 != K:
+        raise ValueError("A and Bt disagree on K")
+    if C is None and C_f32_check is None:
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    c_dtype, ldc = IGC_F32, 0
+    if C is not None:
+        m, n, ldc = _rows(C, "C", (torch.bfloat16, torch.float32))
+        if (m, n) != (M, N):
+            raise ValueError("C has the wrong shape")
+        c_dtype = IGC_BF16 if C.dtype == torch.bfloat16 else IGC_F32
+    ldc32 = 0
+    if C_f32_check is not None:
+        m, n, ldc32 = _rows(C_f32_check, "C_f32_check", torch.float32)
+        if (m, n) != (M, N):
+            raise ValueError("C_f32_check has the wrong shape")
+    rc = lib().gemm_bf16(M, N, K, _ptr(A), lda, _ptr(Bt), ldb, _ptr(C), ldc, c_dtype,
+                         _ptr(C_f32_check), ldc32, _stream(stream))
+    _check(rc, "gemm_bf16")
+    return C
+
+
 def gemm_s8_zp_workspace_size(M: int, N: int, K: int) -> int:
     return int(lib().gemm_s8_zp_workspace_size(M, N, K))
 
@@ -228,6 +262,38 @@ def gemm_s8_zp(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, C32=None, C8=None,
                           _stream(stream))
     _check(rc, "gemm_s8_zp")
     return C32, C8
+
+
+def gemm_s8_zp_dequant(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, scale_row=None,
+                       scale_col=None, bias=None, Y=None, workspace=None, stream=None):
+    """INT8 GEMM with zero points and a dequantised fp32 output
+    Y = ((fp32(C32) * scale_row_i) * scale_col_j) + bias_j.  Returns Y."""
+    import torch
+    M, K, lda = _rows(A, "A", (torch.uint8, torch.int8))
+    N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8))
+    if K2 != K:
+        raise ValueError("A and Bt disagree on K")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    m, n, ldy = _rows(Y, "Y", torch.float32)
+    if (m, n) != (M, N):
+        raise ValueError("Y has the wrong shape")
+    for v, name, n_, dt in ((zA_row, "zA_row", M, torch.int32), (zB_col, "zB_col", N, torch.int32),
+                            (scale_row, "scale_row", M, torch.float32),
+                            (scale_col, "scale_col", N, torch.float32), (bias, "bias", N, torch.float32)):
+        if v is not None and (v.dtype != dt or v.numel() != n_ or not v.is_contiguous() or not v.is_cuda):
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} vector of length {n_}")
+    if workspace is None:
+        workspace = torch.empty(max(gemm_s8_zp_workspace_size(M, N, K), 1), dtype=torch.uint8,
+                                device=A.device)
+    rc = lib().gemm_s8_zp_dequant(M, N, K, _ptr(A), 1 if A.dtype == torch.int8 else 0, lda,
+                                  _ptr(Bt), 1 if Bt.dtype == torch.int8 else 0, ldb,
+                                  int(zA), _ptr(zA_row), int(zB), _ptr(zB_col),
+                                  _ptr(scale_row), _ptr(scale_col), _ptr(bias), _ptr(Y), ldy,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    _check(rc, "gemm_s8_zp_dequant")
+    return Y
 
 
 IGC_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

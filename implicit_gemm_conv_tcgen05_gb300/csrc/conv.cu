@@ -69,7 +69,7 @@ extern "C" int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R
   p.stride_w = stride_w;
   p.out = y;
   p.ldo = K;
-  p.out_f16 = 1;
+  p.out_type = kOutF16;
   p.out_f32 = y_f32_check;
   p.ldo32 = K;
   p.vec_ok = vec_store_ok(y, K, 2) && vec_store_ok(y_f32_check, K, 4);

@@ -43,7 +43,7 @@ extern "C" int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   p.chunk_kb = p.num_kb;
   p.out = C;
   p.ldo = ldc;
-  p.out_f16 = c_dtype == IGC_F16 ? 1 : 0;
+  p.out_type = c_dtype == IGC_F16 ? kOutF16 : kOutF32;
   p.out_f32 = C_f32_check;
   p.ldo32 = ldc32;
   p.vec_ok = vec_store_ok(C, ldc, esize) && vec_store_ok(C_f32_check, ldc32, 4);

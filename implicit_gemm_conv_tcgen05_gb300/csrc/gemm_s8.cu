@@ -223,23 +223,34 @@ extern "C" int gemm_s8_zp_prepare(int64_t M, int64_t N, int64_t K, const void* A
   return launch_prepass(ops, n_ops, K, Kp, stream);
 }
 
-extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
-                              int32_t zA, const int32_t* zA_row, int32_t zB,
-                              const int32_t* zB_col, int32_t* C32, int64_t ldc32, int8_t* C8,
-                              int64_t ldc8, float scale, const float* scale_col,
-                              const void* workspace, size_t workspace_bytes,
-                              igc_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+namespace {
+
+struct DequantOut {
+  float* y = nullptr;
+  long long ldy = 0;
+  const float* dq_row = nullptr;
+  const float* dq_col = nullptr;
+  const float* bias = nullptr;
+};
+
+int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, int32_t zA,
+                 const int32_t* zA_row, int32_t zB, const int32_t* zB_col, int32_t* C32,
+                 int64_t ldc32, int8_t* C8, int64_t ldc8, float scale, const float* scale_col,
+                 const DequantOut& dq, const void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
   int rc = check_common(M, N, K);
   if (rc != IGC_OK) return rc;
   if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
-  if (C32 == nullptr && C8 == nullptr) return IGC_ERR_INVALID_ARG;
+  if (C32 == nullptr && C8 == nullptr && dq.y == nullptr) return IGC_ERR_INVALID_ARG;
   if (C32 != nullptr && ldc32 < N) return IGC_ERR_INVALID_ARG;
   if (C8 != nullptr && ldc8 < N) return IGC_ERR_INVALID_ARG;
+  if (dq.y != nullptr && dq.ldy < N) return IGC_ERR_INVALID_ARG;
   DeviceInfo dev;
   rc = current_device(&dev);
   if (rc != IGC_OK) return rc;
-  if (K == 0) {  // empty sum: C32 = 0 and C8 = requant(0) = 0; nothing is read
+  if (K == 0) {
+    if (dq.y != nullptr) return IGC_ERR_UNSUPPORTED;  // a dequantised output needs K >= 1
+    // empty sum: C32 = 0 and C8 = requant(0) = 0; nothing is read
     rc = zero_rows(C32, ldc32, M, N, 4, stream);
     if (rc == IGC_OK) rc = zero_rows(C8, ldc8, M, N, 1, stream);
     return rc;
@@ -275,8 +286,54 @@ extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int
   p.oB = b_signed ? 0 : 128;
   p.scale = scale;
   p.scale_col = scale_col;
-  p.vec_ok = vec_store_ok(C32, ldc32, 4) && vec_store_ok(C8, ldc8, 1);
+  p.yf = dq.y;
+  p.ldyf = dq.ldy;
+  p.dq_row = dq.dq_row;
+  p.dq_col = dq.dq_col;
+  p.bias = dq.bias;
+  p.vec_ok = vec_store_ok(C32, ldc32, 4) && vec_store_ok(C8, ldc8, 1) &&
+             vec_store_ok(dq.y, dq.ldy, 4);
   return launch_auto_bn<Mode::GemmInt>(dev, tmA, ws + l.b_off, Kp, N, Kp * 2, p, stream);
+}
+
+}  // namespace
+
+extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
+                              int32_t zA, const int32_t* zA_row, int32_t zB,
+                              const int32_t* zB_col, int32_t* C32, int64_t ldc32, int8_t* C8,
+                              int64_t ldc8, float scale, const float* scale_col,
+                              const void* workspace, size_t workspace_bytes,
+                              igc_stream_t stream) {
+  return run_int_gemm(M, N, K, a_signed, b_signed, zA, zA_row, zB, zB_col, C32, ldc32, C8, ldc8,
+                      scale, scale_col, DequantOut(), workspace, workspace_bytes,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gemm_s8_zp_dequant(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,
+                                  int64_t lda, const void* Bt, int b_signed, int64_t ldb,
+                                  int32_t zA, const int32_t* zA_row, int32_t zB,
+                                  const int32_t* zB_col, const float* scale_row,
+                                  const float* scale_col, const float* bias, float* Y,
+                                  int64_t ldy, void* workspace, size_t workspace_bytes,
+                                  igc_stream_t stream) {
+  int rc = check_common(M, N, K);
+  if (rc != IGC_OK) return rc;
+  if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
+  if (Y == nullptr || ldy < N) return IGC_ERR_INVALID_ARG;
+  if (K == 0) return IGC_ERR_UNSUPPORTED;
+  if (A == nullptr || Bt == nullptr) return IGC_ERR_INVALID_ARG;
+  rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,
+                          workspace_bytes, stream);
+  if (rc != IGC_OK) return rc;
+  DequantOut dq;
+  dq.y = Y;
+  dq.ldy = ldy;
+  dq.dq_row = scale_row;
+  dq.dq_col = scale_col;
+  dq.bias = bias;
+  return run_int_gemm(M, N, K, a_signed, b_signed, zA, zA_row, zB, zB_col, nullptr, 0, nullptr,
+                      0, 0.0f, nullptr, dq, workspace, workspace_bytes,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_signed,

@@ -38,13 +38,17 @@
 // into an int32 running sum with the round-to-integer trick x + 1.5*2^23.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "sm100_ptx.cuh"
 
 namespace igc {
 
-enum class Mode : int { GemmF16 = 0, ConvF16 = 1, GemmInt = 2 };
+enum class Mode : int { GemmF16 = 0, ConvF16 = 1, GemmInt = 2, GemmBF16 = 3 };
+
+// element type of the floating output
+enum : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
 constexpr int BM = 256;        // rows per cluster tile (128 per CTA)
 constexpr int BM_CTA = 128;
@@ -104,7 +108,7 @@ struct KParams {
   int pad_h, pad_w, stride_h, stride_w;
   void* out;
   long long ldo;
-  int out_f16;
+  int out_type;  // kOutF32 / kOutF16 / kOutBF16
   float* out_f32;
   long long ldo32;
   int vec_ok;
@@ -121,6 +125,12 @@ struct KParams {
   int32_t oA, oB;
   float scale;
   const float* scale_col;
+  // dequantised float output of the int8 path: y = ((fp32(C32) * dq_row_i) * dq_col_j) + bias_j
+  float* yf;
+  long long ldyf;
+  const float* dq_row;
+  const float* dq_col;
+  const float* bias;
   unsigned long long wait_limit_ns;
   unsigned long long* status;
 };
@@ -143,56 +153,71 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo_bits, uint32_t hi_bit
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_bf162(uint32_t lo_bits, uint32_t hi_bits) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits) {
+  if constexpr (kBf16)
+    return pack_bf162(lo_bits, hi_bits);
+  else
+    return pack_half2(lo_bits, hi_bits);
+}
+
+template <int NC, bool kBf16>
+__device__ __forceinline__ void store_row_16bit(void* out, long long ldo, int M, int N, int m,
+                                                int n0, bool full, const uint32_t (&v)[NC]) {
+  uint16_t* row = reinterpret_cast<uint16_t*>(out) + static_cast<size_t>(m) * ldo + n0;
+  if (full) {
+#pragma unroll
+    for (int j = 0; j < NC / 8; ++j) {
+      uint4 q;
+      q.x = pack2<kBf16>(v[8 * j + 0], v[8 * j + 1]);
+      q.y = pack2<kBf16>(v[8 * j + 2], v[8 * j + 3]);
+      q.z = pack2<kBf16>(v[8 * j + 4], v[8 * j + 5]);
+      q.w = pack2<kBf16>(v[8 * j + 6], v[8 * j + 7]);
+      reinterpret_cast<uint4*>(row)[j] = q;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NC; ++i)
+      if (n0 + i < N) row[i] = static_cast<uint16_t>(pack2<kBf16>(v[i], 0u) & 0xFFFFu);
+  }
+}
+
+template <int NC>
+__device__ __forceinline__ void store_row_f32(float* out, long long ldo, int N, int m, int n0,
+                                              bool full, const uint32_t (&v)[NC]) {
+  float* row = out + static_cast<size_t>(m) * ldo + n0;
+  if (full) {
+#pragma unroll
+    for (int j = 0; j < NC / 4; ++j)
+      reinterpret_cast<uint4*>(row)[j] =
+          make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NC; ++i)
+      if (n0 + i < N) row[i] = __uint_as_float(v[i]);
+  }
+}
+
+// Row m of the tile, columns n0 .. n0+NC-1, values v (fp32 bit patterns).
 template <int NC>
 __device__ __forceinline__ void store_row_float(const KParams& p, int m, int n0,
                                                 const uint32_t (&v)[NC]) {
   if (m >= p.M) return;
   const bool full = p.vec_ok && (n0 + NC <= p.N);
   if (p.out != nullptr) {
-    if (p.out_f16) {
-      __half* row = reinterpret_cast<__half*>(p.out) + static_cast<size_t>(m) * p.ldo + n0;
-      if (full) {
-#pragma unroll
-        for (int j = 0; j < NC / 8; ++j) {
-          uint4 q;
-          q.x = pack_half2(v[8 * j + 0], v[8 * j + 1]);
-          q.y = pack_half2(v[8 * j + 2], v[8 * j + 3]);
-          q.z = pack_half2(v[8 * j + 4], v[8 * j + 5]);
-          q.w = pack_half2(v[8 * j + 6], v[8 * j + 7]);
-          reinterpret_cast<uint4*>(row)[j] = q;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < NC; ++i)
-          if (n0 + i < p.N) row[i] = __float2half_rn(__uint_as_float(v[i]));
-      }
-    } else {
-      float* row = reinterpret_cast<float*>(p.out) + static_cast<size_t>(m) * p.ldo + n0;
-      if (full) {
-#pragma unroll
-        for (int j = 0; j < NC / 4; ++j)
-          reinterpret_cast<uint4*>(row)[j] =
-              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < NC; ++i)
-          if (n0 + i < p.N) row[i] = __uint_as_float(v[i]);
-      }
-    }
+    if (p.out_type == kOutF16)
+      store_row_16bit<NC, false>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
+    else if (p.out_type == kOutBF16)
+      store_row_16bit<NC, true>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
+    else
+      store_row_f32<NC>(reinterpret_cast<float*>(p.out), p.ldo, p.N, m, n0, full, v);
   }
-  if (p.out_f32 != nullptr) {
-    float* row = p.out_f32 + static_cast<size_t>(m) * p.ldo32 + n0;
-    if (full) {
-#pragma unroll
-      for (int j = 0; j < NC / 4; ++j)
-        reinterpret_cast<uint4*>(row)[j] =
-            make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < NC; ++i)
-        if (n0 + i < p.N) row[i] = __uint_as_float(v[i]);
-    }
-  }
+  if (p.out_f32 != nullptr) store_row_f32<NC>(p.out_f32, p.ldo32, p.N, m, n0, full, v);
 }
 
 __device__ __forceinline__ int8_t requant_i8(int32_t c, float s) {
@@ -215,6 +240,8 @@ __device__ __forceinline__ void store_row_int(const KParams& p, int m, int n0,
   const bool full = p.vec_ok && (n0 + NC <= p.N);
   int32_t* row32 = p.c32 ? p.c32 + static_cast<size_t>(m) * p.ldc32 + n0 : nullptr;
   int8_t* row8 = p.c8 ? p.c8 + static_cast<size_t>(m) * p.ldc8 + n0 : nullptr;
+  float* rowf = p.yf ? p.yf + static_cast<size_t>(m) * p.ldyf + n0 : nullptr;
+  const float sA = p.dq_row ? __ldg(p.dq_row + m) : 1.0f;
 #pragma unroll
   for (int j = 0; j < NC / 16; ++j) {
     int32_t c[16];
@@ -238,6 +265,30 @@ __device__ __forceinline__ void store_row_int(const KParams& p, int m, int n0,
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           if (n0 + j * 16 + i < p.N) row32[j * 16 + i] = c[i];
+      }
+    }
+    if (rowf) {
+      // dequantise: one RNE fp32 operation per step, in this order, no FMA
+      float y[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int n = n0 + j * 16 + i;
+        const int nn = n < p.N ? n : p.N - 1;
+        float t = __int2float_rn(c[i]);
+        if (p.dq_row) t = __fmul_rn(t, sA);
+        if (p.dq_col) t = __fmul_rn(t, __ldg(p.dq_col + nn));
+        if (p.bias) t = __fadd_rn(t, __ldg(p.bias + nn));
+        y[i] = t;
+      }
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<float4*>(rowf + j * 16)[i] =
+              make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (n0 + j * 16 + i < p.N) rowf[j * 16 + i] = y[i];
       }
     }
     if (row8) {
@@ -461,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (leader)
     // The whole warp runs the loop (converged); lane 0 issues MMAs and commits.
     if (rank == 0) {
-      constexpr uint32_t idesc = make_idesc_f16_f32(BM, BN);
+      constexpr uint32_t idesc = make_idesc_kind_f16(BM, BN, kMode == Mode::GemmBF16 ? 1u : 0u);
       // descriptors of stage 0, atom 0, k 0; the start-address field (bits 0-13,
       // in 16-byte units) is advanced by adding offsets >> 4 (no carry: < 256 KB)
       const uint64_t adesc0 = make_sw128_kmajor_desc(smem_u32(sA));

@@ -137,12 +137,15 @@ template <Mode kMode>
 int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_base,
                    uint64_t b_inner, uint64_t b_rows, uint64_t b_row_bytes, KParams p,
                    cudaStream_t stream) {
+  constexpr CUtensorMapDataType kBType = kMode == Mode::GemmBF16
+                                             ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   int clusters = 0;
   int rc = kernel_setup<kMode, kBnCands[0]>(dev, &clusters);
   if (rc != IGC_OK) return rc;
   const int bn = pick_bn(p.M, p.N, clusters, kBnCands, kBnEff, kNumBn);
   CUtensorMap tmB;
-  rc = encode_tiled_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b_base, b_inner, b_rows,
+  rc = encode_tiled_2d(&tmB, kBType, b_base, b_inner, b_rows,
                        b_row_bytes, BK, static_cast<uint32_t>(bn / 2));
   if (rc != IGC_OK) return rc;
   switch (bn) {

@@ -357,12 +357,13 @@ __device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor for kind::f16: fp16 A and B (both K-major), fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16), 10-12 B format,
-//   15/16 A/B major (0 = K-major), 17-22 N >> 3, 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t make_idesc_f16_f32(int m, int n) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// Instruction descriptor for kind::f16 with fp32 D, both operands K-major.
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B always share one type), 15/16 A/B major (0 = K-major),
+//   17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc_kind_f16(int m, int n, uint32_t ab_format) {
+  return (1u << 4) | (ab_format << 7) | (ab_format << 10) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 }  // namespace igc

@@ -56,9 +56,10 @@ typedef struct CUstream_st *igc_stream_t;
 #define IGC_ERR_DEVICE_TIMEOUT 5 /* a kernel's bounded pipeline wait gave up */
 #define IGC_ERR_WORKSPACE 6      /* workspace pointer null or smaller than required */
 
-/* output element types for gemm_f16 */
+/* output element types for gemm_f16 / gemm_bf16 */
 #define IGC_F32 0
 #define IGC_F16 1
+#define IGC_BF16 2
 
 /*
  * gemm_f16 -- C = A * B, fp16 operands, fp32 accumulation ([P1] §4.1, §2.1).
@@ -87,6 +88,24 @@ int gemm_f16(int64_t M, int64_t N, int64_t K,
              void *C, int64_t ldc, int c_dtype,
              float *C_f32_check, int64_t ldc32,
              igc_stream_t stream);
+
+/*
+ * gemm_bf16 -- gemm_f16 with bf16 operands ([P1] §3.3: the f16 -> bf16 swap of
+ * the tensor intrinsic), fp32 accumulation on the same tensor pipe.
+ *
+ *   C[i,j] = sum_{k<K} A[i,k] * Bt[j,k]
+ *
+ *  A, Bt as for gemm_f16 but bf16.  C is IGC_F32 (the accumulator) or IGC_BF16
+ *  (round to nearest even of the fp32 accumulator); C_f32_check as for
+ *  gemm_f16.  Sizes, alignment and accuracy bound as for gemm_f16, plus the
+ *  bf16 rounding of C when c_dtype is IGC_BF16.
+ */
+int gemm_bf16(int64_t M, int64_t N, int64_t K,
+              const void *A, int64_t lda,
+              const void *Bt, int64_t ldb,
+              void *C, int64_t ldc, int c_dtype,
+              float *C_f32_check, int64_t ldc32,
+              igc_stream_t stream);
 
 /*
  * gemm_s8_zp -- INT8 GEMM with input zero points and requantisation
@@ -164,6 +183,31 @@ int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
                    float scale, const float *scale_col,
                    const void *workspace, size_t workspace_bytes,
                    igc_stream_t stream);
+
+/*
+ * gemm_s8_zp_dequant -- INT8 GEMM with zero points and a dequantised float
+ * output, the "dequantize(C) + add_bias" half of [P1] §2.3's four-term fusion:
+ *
+ *   C32[i,j] = sum_{k<K} (A_q[i,k] - zA_i) * (B_q[k,j] - zB_j)          (int32)
+ *   Y[i,j]   = ((fp32(C32[i,j]) * scale_row_i) * scale_col_j) + bias_j  (fp32)
+ *
+ * Each step is one fp32 operation rounded to nearest even, in this order, with
+ * no fused multiply-add; a NULL scale_row / scale_col / bias vector skips its
+ * step (scale 1, bias 0).  scale_row is device float[M] (the per-row scale of
+ * A), scale_col and bias device float[N] (per-column scale of B, bias).
+ * Y is device fp32 M x N row-major (row stride ldy >= N).  The other arguments,
+ * the workspace, alignment and sizes are as for gemm_s8_zp, except that K must
+ * be >= 1 (IGC_ERR_UNSUPPORTED otherwise).  Results are bit-exact.
+ */
+int gemm_s8_zp_dequant(int64_t M, int64_t N, int64_t K,
+                       const void *A, int a_signed, int64_t lda,
+                       const void *Bt, int b_signed, int64_t ldb,
+                       int32_t zA, const int32_t *zA_row,
+                       int32_t zB, const int32_t *zB_col,
+                       const float *scale_row, const float *scale_col, const float *bias,
+                       float *Y, int64_t ldy,
+                       void *workspace, size_t workspace_bytes,
+                       igc_stream_t stream);
 
 /*
  * gemm_s8_zp_noalloc -- gemm_s8_zp without a caller-provided workspace, for

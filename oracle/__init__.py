@@ -53,6 +53,16 @@ def lib() -> ctypes.CDLL:
             L.oracle_f32_to_f16_rne.restype = ctypes.c_uint16
             L.oracle_f32_to_f16_rne_array.argtypes = [vp, vp, i64]
             L.oracle_f32_to_f16_rne_array.restype = None
+            L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_to_f64.restype = ctypes.c_double
+            L.oracle_f32_to_bf16_rne_array.argtypes = [vp, vp, i64]
+            L.oracle_f32_to_bf16_rne_array.restype = None
+            L.oracle_gemm_bf16.argtypes = [i64, i64, i64, vp, i64, vp, i64, dp, dp, i32]
+            L.oracle_gemm_bf16.restype = i32
+            L.oracle_dequant.argtypes = [ctypes.c_int32, vp, vp, vp]
+            L.oracle_dequant.restype = ctypes.c_float
+            L.oracle_dequant_matrix.argtypes = [i64, i64, vp, vp, vp, vp, vp]
+            L.oracle_dequant_matrix.restype = None
             L.oracle_i32_to_f32_rne.argtypes = [ctypes.c_int32]
             L.oracle_i32_to_f32_rne.restype = ctypes.c_float
             L.oracle_requant.argtypes = [ctypes.c_int32, ctypes.c_float]
@@ -106,6 +116,49 @@ def f32_to_f16_array(x: np.ndarray) -> np.ndarray:
     out = np.empty(flat.size, np.uint16)
     lib().oracle_f32_to_f16_rne_array(_ptr(flat), _ptr(out), flat.size)
     return out.view(np.float16).reshape(np.shape(x))
+
+
+def bf16_to_f64(bits: int) -> float:
+    return float(lib().oracle_bf16_to_f64(int(bits) & 0xFFFF))
+
+
+def f32_to_bf16_bits_array(x: np.ndarray) -> np.ndarray:
+    """Round an fp32 array to bf16 (RNE) with the oracle's own conversion; returns uint16 bits."""
+    flat = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.empty(flat.size, np.uint16)
+    lib().oracle_f32_to_bf16_rne_array(_ptr(flat), _ptr(out), flat.size)
+    return out.reshape(np.shape(x))
+
+
+def gemm_bf16(A_bits: np.ndarray, Bt_bits: np.ndarray, nthreads: int = 0):
+    """ref and sabs in double from bf16 operands given as uint16 bit arrays (M x K, N x K)."""
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    Bt = np.ascontiguousarray(Bt_bits, dtype=np.uint16)
+    M, K = A.shape
+    N, K2 = Bt.shape
+    assert K == K2
+    ref = np.empty((M, N), np.float64)
+    sabs = np.empty((M, N), np.float64)
+    rc = lib().oracle_gemm_bf16(M, N, K, _ptr(A), K, _ptr(Bt), K, _ptr(ref), _ptr(sabs), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_gemm_bf16: bad arguments")
+    return ref, sabs
+
+
+def dequant(c32: int, s_row=None, s_col=None, bias=None) -> float:
+    """One dequantised output value; None skips a step."""
+    f = lambda v: None if v is None else ctypes.byref(ctypes.c_float(v))  # noqa: E731
+    return float(lib().oracle_dequant(int(c32), f(s_row), f(s_col), f(bias)))
+
+
+def dequant_matrix(C32: np.ndarray, s_row=None, s_col=None, bias=None) -> np.ndarray:
+    C32 = np.ascontiguousarray(C32, dtype=np.int32)
+    M, N = C32.shape
+    conv = lambda v: None if v is None else np.ascontiguousarray(v, dtype=np.float32)  # noqa: E731
+    s_row, s_col, bias = conv(s_row), conv(s_col), conv(bias)
+    Y = np.empty((M, N), np.float32)
+    lib().oracle_dequant_matrix(M, N, _ptr(C32), _ptr(s_row), _ptr(s_col), _ptr(bias), _ptr(Y))
+    return Y
 
 
 def conv_out_dim(n: int, filt: int, pad: int, stride: int) -> int:

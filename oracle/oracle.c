@@ -115,6 +115,36 @@ void oracle_f32_to_f16_rne_array(const float *in, uint16_t *out, int64_t n)
         out[i] = oracle_f32_to_f16_rne(in[i]);
 }
 
+/* bfloat16 bits (the top half of a binary32) -> exact double value. */
+double oracle_bf16_to_f64(uint16_t h)
+{
+    uint32_t x = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &x, 4);
+    return (double)f;
+}
+
+/* binary32 value -> bfloat16 bits, round to nearest, ties to even on the 16
+ * dropped bits; NaN stays a (quiet) NaN, overflow rounds to +-inf. */
+uint16_t oracle_f32_to_bf16_rne(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    if ((x & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((x >> 16) | 0x0040u);
+    uint32_t hi = x >> 16;
+    uint32_t rem = x & 0xffffu;
+    if (rem > 0x8000u || (rem == 0x8000u && (hi & 1u)))
+        hi += 1;                                      /* carries into the exponent correctly */
+    return (uint16_t)hi;
+}
+
+void oracle_f32_to_bf16_rne_array(const float *in, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f32_to_bf16_rne(in[i]);
+}
+
 /* int32 -> binary32, round to nearest, ties to even. */
 float oracle_i32_to_f32_rne(int32_t v)
 {
@@ -163,6 +193,31 @@ int8_t oracle_requant(int32_t c32, float scale)
     if (r < -128)
         r = -128;
     return (int8_t)r;
+}
+
+/* Dequantised float output of the int8 GEMM ([P1] §2.3's dequantize(C) +
+ * add_bias; order and precision as read above): each step one fp32 operation
+ * rounded to nearest even, a NULL pointer skips its step. */
+float oracle_dequant(int32_t c32, const float *s_row, const float *s_col, const float *bias)
+{
+    float t = oracle_i32_to_f32_rne(c32);
+    if (s_row)
+        t = t * *s_row;
+    if (s_col)
+        t = t * *s_col;
+    if (bias)
+        t = t + *bias;
+    return t;
+}
+
+/* Y[i,j] = oracle_dequant(C32[i,j], s_row[i], s_col[j], bias[j]) over an M x N matrix. */
+void oracle_dequant_matrix(int64_t M, int64_t N, const int32_t *C32, const float *s_row,
+                           const float *s_col, const float *bias, float *Y)
+{
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            Y[i * N + j] = oracle_dequant(C32[i * N + j], s_row ? s_row + i : NULL,
+                                          s_col ? s_col + j : NULL, bias ? bias + j : NULL);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -277,6 +332,46 @@ int oracle_gemm_f16(int64_t M, int64_t N, int64_t K,
             Bd[j * K + k] = oracle_f16_to_f64(Bt[j * ldb + k]);
     struct gemm_f16_ctx c = {N, K, A, lda, Bd, ref, sabs, N};
     parallel_rows(M, nthreads, gemm_f16_row, &c);
+    free(Bd);
+    return 0;
+}
+
+/* BF16 GEMM ([P1] §3.3's f16 -> bf16 swap of the same definition):
+ * ref[i,j] = sum_k A[i,k] * Bt[j,k] in double from bf16 operands, sabs likewise. */
+int oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
+                     const uint16_t *A, int64_t lda,
+                     const uint16_t *Bt, int64_t ldb,
+                     double *ref, double *sabs, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || !ref)
+        return -1;
+    double *Ad = (double *)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    double *Bd = (double *)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!Ad || !Bd) {
+        free(Ad);
+        free(Bd);
+        return -1;
+    }
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t k = 0; k < K; ++k)
+            Ad[i * K + k] = oracle_bf16_to_f64(A[i * lda + k]);
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t k = 0; k < K; ++k)
+            Bd[j * K + k] = oracle_bf16_to_f64(Bt[j * ldb + k]);
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0, sa = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double prod = Ad[i * K + k] * Bd[j * K + k];
+                acc += prod;
+                sa += fabs(prod);
+            }
+            ref[i * N + j] = acc;
+            if (sabs)
+                sabs[i * N + j] = sa;
+        }
+    (void)nthreads;
+    free(Ad);
     free(Bd);
     return 0;
 }

@@ -40,7 +40,7 @@ import numpy as np
 
 __all__ = [
     "SEED_BASE", "seed_for", "splitmix64", "hashes", "uniform01",
-    "uniform_f16", "normal_f16", "uniform_int", "uniform_f32",
+    "uniform_f16", "normal_f16", "normal_bf16_bits", "uniform_int", "uniform_f32",
     "gemm_f16_inputs", "gemm_s8_inputs", "conv_inputs", "workload",
     "WORKLOADS",
 ]
@@ -110,6 +110,21 @@ def normal_f16(seed: int, tid: int, shape, std: float = 1.0) -> np.ndarray:
         z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
         return (std * z).astype(np.float16)
     return _fill(n, fn, np.float16).reshape(shape)
+
+
+def normal_bf16_bits(seed: int, tid: int, shape, std: float = 1.0) -> np.ndarray:
+    """N(0, std) drawn in float64, rounded once to bfloat16 (RNE, by torch's
+    conversion); returned as the uint16 bit patterns."""
+    import torch
+    n = int(np.prod(shape))
+
+    def fn(s, c):
+        h = hashes(seed, tid, 2 * s, 2 * c)
+        u1 = ((h[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+        u2 = (h[1::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        z = std * np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+        return torch.from_numpy(z).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return _fill(n, fn, np.uint16).reshape(shape)
 
 
 def uniform_int(seed: int, tid: int, shape, lo: int, hi: int, dtype) -> np.ndarray:

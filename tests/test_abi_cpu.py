@@ -13,8 +13,8 @@ import implicit_gemm_conv_tcgen05_gb300 as igc
 def test_library_loads_and_exports_every_declared_symbol():
     L = igc.lib()
     names = igc.declared_functions()
-    expected = {"gemm_f16", "gemm_s8_zp", "gemm_s8_zp_workspace_size", "gemm_s8_zp_prepare",
-                "gemm_s8_zp_run", "conv2d_nhwc_f16_implicit",
+    expected = {"gemm_f16", "gemm_bf16", "gemm_s8_zp", "gemm_s8_zp_workspace_size", "gemm_s8_zp_prepare",
+                "gemm_s8_zp_run", "gemm_s8_zp_dequant", "gemm_s8_zp_noalloc", "conv2d_nhwc_f16_implicit",
                 "igc_status_string", "igc_check_device_status", "igc_last_device_status",
                 "igc_set_wait_limit_ns", "igc_debug_wait_timeout_probe", "igc_version"}
     assert expected <= set(names)
@@ -88,6 +88,6 @@ def test_header_declares_c_linkage_and_statuses():
     assert 'extern "C"' in text
     for name, code in [("IGC_OK", 0), ("IGC_ERR_INVALID_ARG", 1), ("IGC_ERR_MISALIGNED", 2),
                        ("IGC_ERR_UNSUPPORTED", 3), ("IGC_ERR_CUDA", 4), ("IGC_ERR_DEVICE_TIMEOUT", 5),
-                       ("IGC_ERR_WORKSPACE", 6)]:
+                       ("IGC_ERR_WORKSPACE", 6), ("IGC_F32", 0), ("IGC_F16", 1), ("IGC_BF16", 2)]:
         assert re.search(rf"#define {name} {code}\b", text)
         assert getattr(igc, name) == code

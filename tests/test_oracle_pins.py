@@ -349,3 +349,87 @@ def test_generators_are_counter_based_and_in_range():
     assert u.min() >= -1 and u.max() <= 1 and abs(u.mean()) < 0.01
     sc = synth.uniform_f32(4, 6, (10000,), 1e-4, 1e-3)
     assert sc.dtype == np.float32 and sc.min() >= np.float32(1e-4) and sc.max() <= np.float32(1e-3)
+
+
+# ---------------------------------------------------------------------------
+# bf16 (the f16 -> bf16 swap of the GEMM)
+# ---------------------------------------------------------------------------
+
+def _bits_to_bf16_tensor(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def test_bf16_decode_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = _bits_to_bf16_tensor(bits).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_f64(int(b)) for b in bits])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_f32_to_bf16_rne_matches_library_conversion():
+    x = _f32_samples()
+    got = oracle.f32_to_bf16_bits_array(x)
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(x)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.all(np.isnan(_bits_to_bf16_tensor(got[nan]).to(torch.float32).numpy()))
+
+
+def test_gemm_bf16_exact_cases_and_float64_matmul():
+    rng = np.random.default_rng(3)
+    M, N, K = 37, 45, 300
+    A = rng.integers(-3, 4, size=(M, K))
+    Bt = rng.integers(-3, 4, size=(N, K))
+    to_bits = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    ref, sabs = oracle.gemm_bf16(to_bits(A), to_bits(Bt))
+    assert np.array_equal(ref, (A @ Bt.T).astype(np.float64))
+    assert np.array_equal(sabs, (np.abs(A) @ np.abs(Bt).T).astype(np.float64))
+    eye = np.eye(64)
+    B = synth.normal_bf16_bits(4, 2, (64, 64))
+    ref, _ = oracle.gemm_bf16(to_bits(eye), B)
+    assert np.array_equal(ref, _bits_to_bf16_tensor(B).to(torch.float64).numpy().T)
+    A2 = synth.normal_bf16_bits(5, 1, (19, 70))
+    B2 = synth.normal_bf16_bits(5, 2, (23, 70))
+    ref, _ = oracle.gemm_bf16(A2, B2)
+    want = (_bits_to_bf16_tensor(A2).double() @ _bits_to_bf16_tensor(B2).double().T).numpy()
+    assert np.allclose(ref, want, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# dequantised float output (four-term fusion)
+# ---------------------------------------------------------------------------
+
+def _f32_from_bits(h):
+    return struct.unpack("<f", struct.pack("<I", int(h, 16)))[0]
+
+
+def test_dequant_hand_table():
+    n = 0
+    with open(os.path.join(GOLDEN, "dequant_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            c32, sr, sc, b, want = line.split()[:5]
+            args = [None if v == "-" else _f32_from_bits(v) for v in (sr, sc, b)]
+            got = oracle.dequant(int(c32), *args)
+            assert struct.pack("<f", got) == struct.pack("<I", int(want, 16)), line
+            n += 1
+    assert n >= 7
+
+
+def test_dequant_closed_forms():
+    rng = np.random.default_rng(8)
+    C32 = rng.integers(-2**23, 2**23, size=(7, 11)).astype(np.int32)
+    # no steps: exactly the int32 values (all below 2^24)
+    assert np.array_equal(oracle.dequant_matrix(C32), C32.astype(np.float32))
+    # power-of-two scales: exact scaling; small-integer bias: exact shift
+    s_row = np.exp2(rng.integers(-8, 3, size=7)).astype(np.float32)
+    s_col = np.exp2(rng.integers(-8, 3, size=11)).astype(np.float32)
+    bias = rng.integers(-100, 100, size=11).astype(np.float32)
+    want = (C32.astype(np.float64) * s_row[:, None] * s_col[None, :]) + bias[None, :]
+    got = oracle.dequant_matrix(C32, s_row, s_col, bias)
+    exact = np.abs(want) < 2**24
+    assert np.array_equal(got[exact].astype(np.float64), want[exact])
