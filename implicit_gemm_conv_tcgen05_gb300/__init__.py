@@ -83,6 +83,12 @@ def lib() -> ctypes.CDLL:
             L.gemm_s8_zp_workspace_size.restype = sz
             L.conv2d_nhwc_f16_implicit.argtypes = [i32] * 11 + [vp, vp, vp, vp, vp]
             L.conv2d_nhwc_f16_implicit.restype = i32
+            L.conv2d_nhwc_s8_zp.argtypes = [i32] * 11 + [vp, i32, ctypes.c_int32, vp, i32,
+                                                         ctypes.c_int32, vp, vp, vp,
+                                                         ctypes.c_float, vp, vp, sz, vp]
+            L.conv2d_nhwc_s8_zp.restype = i32
+            L.conv2d_nhwc_s8_zp_workspace_size.argtypes = [i32] * 11
+            L.conv2d_nhwc_s8_zp_workspace_size.restype = sz
             L.igc_status_string.argtypes = [i32]
             L.igc_status_string.restype = ctypes.c_char_p
             L.igc_check_device_status.argtypes = [vp]
@@ -381,3 +387,42 @@ def conv2d_nhwc_f16_implicit(x, w, y=None, y_f32_check=None, pad=(1, 1), stride=
                                         _ptr(y), _ptr(y_f32_check), _stream(stream))
     _check(rc, "conv2d_nhwc_f16_implicit")
     return y if y is not None else y_f32_check
+
+
+def conv2d_nhwc_s8_zp_workspace_size(N, H, W, C, K, R, S, pad=(1, 1), stride=(1, 1)) -> int:
+    return int(lib().conv2d_nhwc_s8_zp_workspace_size(N, H, W, C, K, R, S, pad[0], pad[1],
+                                                      stride[0], stride[1]))
+
+
+def conv2d_nhwc_s8_zp(x, w, zX, zW=0, zW_k=None, y32=None, y8=None, scale=0.0, scale_k=None,
+                      pad=(1, 1), stride=(1, 1), workspace=None, stream=None):
+    """INT8 convolution with zero points (padding value zX): x NHWC uint8/int8,
+    w KRSC uint8/int8; outputs y32 (int32) and/or y8 (int8), NPQK.  Returns (y32, y8)."""
+    import torch
+    for t, name in ((x, "x"), (w, "w")):
+        if t.dim() != 4 or t.dtype not in (torch.uint8, torch.int8) or not t.is_contiguous() \
+                or not t.is_cuda:
+            raise ValueError(f"{name} must be a dense 4-D CUDA uint8/int8 tensor")
+    N, H, W, C = x.shape
+    K, R, S, C2 = w.shape
+    if C2 != C:
+        raise ValueError("x and w disagree on C")
+    P = (H + 2 * pad[0] - R) // stride[0] + 1
+    Q = (W + 2 * pad[1] - S) // stride[1] + 1
+    for t, dt, name in ((y32, torch.int32, "y32"), (y8, torch.int8, "y8")):
+        if t is not None and (tuple(t.shape) != (N, P, Q, K) or t.dtype != dt or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a dense ({N},{P},{Q},{K}) {dt} tensor")
+    for v, name, dt in ((zW_k, "zW_k", torch.int32), (scale_k, "scale_k", torch.float32)):
+        if v is not None and (v.dtype != dt or v.numel() != K or not v.is_contiguous() or not v.is_cuda):
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} vector of length {K}")
+    if workspace is None:
+        need = conv2d_nhwc_s8_zp_workspace_size(N, H, W, C, K, R, S, pad, stride)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    rc = lib().conv2d_nhwc_s8_zp(N, H, W, C, K, R, S, pad[0], pad[1], stride[0], stride[1],
+                                 _ptr(x), 1 if x.dtype == torch.int8 else 0, int(zX),
+                                 _ptr(w), 1 if w.dtype == torch.int8 else 0, int(zW), _ptr(zW_k),
+                                 _ptr(y32), _ptr(y8), float(scale), _ptr(scale_k),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream))
+    _check(rc, "conv2d_nhwc_s8_zp")
+    return y32, y8

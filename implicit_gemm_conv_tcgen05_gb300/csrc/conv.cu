@@ -29,7 +29,7 @@ extern "C" int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R
   const long long P = (H + 2LL * pad_h - R) / stride_h + 1;
   const long long Q = (W + 2LL * pad_w - S) / stride_w + 1;
   const long long M = static_cast<long long>(N) * P * Q;
-  if (stride_h != 1 || stride_w != 1) return IGC_ERR_UNSUPPORTED;
+  if (stride_h > 8 || stride_w > 8) return IGC_ERR_UNSUPPORTED;  // TMA traversal stride <= 8
   if (C % 8 != 0) return IGC_ERR_UNSUPPORTED;
   // im2col bounding-box corners of a rank-4 tensor map are limited to [-128, 127]
   const int lower_h = -pad_h, lower_w = -pad_w;

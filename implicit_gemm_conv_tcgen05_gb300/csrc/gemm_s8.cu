@@ -19,9 +19,11 @@
 //     then C8 = clamp(rne(fp32(C32) * scale_j), -128, 127).
 #include <mutex>
 
+#include "int8_prepass.cuh"
 #include "launch.cuh"
 
 using namespace igc;
+using namespace igc::prepass;
 
 namespace {
 
@@ -43,126 +45,6 @@ WsLayout ws_layout(long long M, long long N, long long K) {
   l.cb_off = l.ra_off + align_up(static_cast<size_t>(M) * 4, kWsAlign);
   l.total = l.cb_off + align_up(static_cast<size_t>(N) * 4, kWsAlign);
   return l;
-}
-
-// One operand of the pre-pass: `rows` rows of K bytes (row stride ld), uint8
-// (offset 128) or int8 (offset 0).
-struct PrepassOperand {
-  const uint8_t* src;
-  long long ld;
-  int rows;
-  int is_signed;
-  int offset;
-  int vec;  // K % 16 == 0, 16-byte aligned rows: 16-byte loads
-  __half* dst;
-  int32_t* sums;
-};
-
-struct PrepassParams {
-  PrepassOperand op[2];  // rows of op[0] first, then those of op[1]
-  int K, Kp;
-};
-
-constexpr int kPrepassUnroll = 4;  // 16-byte loads in flight per thread
-
-__device__ __forceinline__ int shifted_byte(uint32_t byte, int is_signed, int offset) {
-  return (is_signed ? static_cast<int>(static_cast<int8_t>(byte)) : static_cast<int>(byte)) -
-         offset;
-}
-
-// One warp per row: dst[row, k] = fp16(src[row, k] - offset) for k < K, 0 for
-// K <= k < Kp; sums[row] = sum_k (src[row, k] - offset).  Both operands of a
-// GEMM go through one launch.
-__global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const PrepassParams pp) {
-  int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
-  const int lane = static_cast<int>(threadIdx.x % 32);
-  // select the operand field by field (a dynamic index into the parameter
-  // struct would copy it to local memory)
-  const bool second = row >= pp.op[0].rows;
-  PrepassOperand o;
-  o.src = second ? pp.op[1].src : pp.op[0].src;
-  o.ld = second ? pp.op[1].ld : pp.op[0].ld;
-  o.rows = second ? pp.op[1].rows : pp.op[0].rows;
-  o.is_signed = second ? pp.op[1].is_signed : pp.op[0].is_signed;
-  o.offset = second ? pp.op[1].offset : pp.op[0].offset;
-  o.vec = second ? pp.op[1].vec : pp.op[0].vec;
-  o.dst = second ? pp.op[1].dst : pp.op[0].dst;
-  o.sums = second ? pp.op[1].sums : pp.op[0].sums;
-  if (second) row -= pp.op[0].rows;
-  if (row >= o.rows) return;
-  const uint8_t* s = o.src + static_cast<size_t>(row) * o.ld;
-  __half* d = o.dst + static_cast<size_t>(row) * pp.Kp;
-  const int K = pp.K;
-  int32_t acc = 0;
-  if (o.vec) {
-    for (int k0 = lane * 16; k0 < K; k0 += 32 * 16 * kPrepassUnroll) {
-      uint4 raw[kPrepassUnroll];
-#pragma unroll
-      for (int u = 0; u < kPrepassUnroll; ++u) {
-        const int k = k0 + u * 32 * 16;
-        raw[u] = k < K ? __ldg(reinterpret_cast<const uint4*>(s + k)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < kPrepassUnroll; ++u) {
-        const int k = k0 + u * 32 * 16;
-        if (k >= K) break;
-        const uint32_t words[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-        uint32_t out[8];
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          int v[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            v[b] = shifted_byte((words[wi] >> (8 * b)) & 0xFFu, o.is_signed, o.offset);
-            acc += v[b];
-          }
-          __half2 h0 = __halves2half2(__int2half_rn(v[0]), __int2half_rn(v[1]));
-          __half2 h1 = __halves2half2(__int2half_rn(v[2]), __int2half_rn(v[3]));
-          out[2 * wi] = *reinterpret_cast<uint32_t*>(&h0);
-          out[2 * wi + 1] = *reinterpret_cast<uint32_t*>(&h1);
-        }
-        reinterpret_cast<uint4*>(d + k)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        reinterpret_cast<uint4*>(d + k)[1] = make_uint4(out[4], out[5], out[6], out[7]);
-      }
-    }
-  } else {
-    for (int k = lane; k < pp.Kp; k += 32) {
-      int v = 0;
-      if (k < K) v = shifted_byte(s[k], o.is_signed, o.offset);
-      acc += v;
-      d[k] = __int2half_rn(v);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) o.sums[row] = acc;
-}
-
-PrepassOperand prepass_operand(const void* src, long long ld, long long rows, long long K,
-                               long long Kp, int is_signed, __half* dst, int32_t* sums) {
-  PrepassOperand o;
-  o.src = static_cast<const uint8_t*>(src);
-  o.ld = ld;
-  o.rows = static_cast<int>(rows);
-  o.is_signed = is_signed;
-  o.offset = is_signed ? 0 : 128;
-  o.vec = (K % 16 == 0) && aligned16(src) && (ld % 16 == 0) && (Kp == K);
-  o.dst = dst;
-  o.sums = sums;
-  return o;
-}
-
-int launch_prepass(const PrepassOperand* ops, int n_ops, long long K, long long Kp,
-                   cudaStream_t stream) {
-  PrepassParams pp{};
-  pp.op[0] = ops[0];
-  if (n_ops > 1) pp.op[1] = ops[1];
-  pp.K = static_cast<int>(K);
-  pp.Kp = static_cast<int>(Kp);
-  const long long rows = static_cast<long long>(pp.op[0].rows) + (n_ops > 1 ? pp.op[1].rows : 0);
-  const long long blocks = (rows + 7) / 8;
-  shift_widen_rowsum_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(pp);
-  return cudaGetLastError() == cudaSuccess ? IGC_OK : IGC_ERR_CUDA;
 }
 
 }  // namespace

@@ -45,7 +45,11 @@
 
 namespace igc {
 
-enum class Mode : int { GemmF16 = 0, ConvF16 = 1, GemmInt = 2, GemmBF16 = 3 };
+enum class Mode : int { GemmF16 = 0, ConvF16 = 1, GemmInt = 2, GemmBF16 = 3, ConvInt = 4 };
+
+// A operand gathered by TMA im2col (a convolution) / integer epilogue
+__host__ __device__ constexpr bool mode_is_conv(Mode m) { return m == Mode::ConvF16 || m == Mode::ConvInt; }
+__host__ __device__ constexpr bool mode_is_int(Mode m) { return m == Mode::GemmInt || m == Mode::ConvInt; }
 
 // element type of the floating output
 enum : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m_cta = mb * BM + static_cast<int>(rank) * BM_CTA;
       const int n_cta = nb * BN + static_cast<int>(rank) * Cfg::kBNHalf;
       int cn = 0, ch = 0, cw = 0;
-      if constexpr (kMode == Mode::ConvF16) {
+      if constexpr (mode_is_conv(kMode)) {
         const int PQ = p.conv_P * p.conv_Q;
         cn = m_cta / PQ;
         const int rem = m_cta - cn * PQ;
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b_dst = sB + stage * Cfg::kStageBBytes;
           const uint32_t bar = full_lead + static_cast<uint32_t>(stage) * 8u;
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * Cfg::kStageBytes);
-          if constexpr (kMode == Mode::ConvF16) {
+          if constexpr (mode_is_conv(kMode)) {
             const int tap = kb / p.conv_cblocks;
             const int c0 = (kb - tap * p.conv_cblocks) * KS;
             const int r = tap / p.conv_S;
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(p, t, mb, nb);
       const int m = mb * BM + static_cast<int>(rank) * BM_CTA + row_in_cta;
       const int n0 = nb * BN + half * NC;
-      if constexpr (kMode != Mode::GemmInt) {
+      if constexpr (!mode_is_int(kMode)) {
         if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag,
                                                         p.status, kSiteEpiFull)))
           goto epi_done;

@@ -260,9 +260,11 @@ int gemm_s8_zp_noalloc(int64_t M, int64_t N, int64_t K,
  *  y    device fp16 NHWC (N x P x Q x K), dense, round to nearest even.  May be
  *       NULL if y_f32_check is given.
  *  y_f32_check  device fp32 N x P x Q x K or NULL: copy of the fp32 accumulator.
- *  Supported: C a multiple of 8 (16-byte pixel rows), stride_h = stride_w = 1,
- *  1 <= R, S <= 8, 0 <= pad <= 7 with pad <= R-1 (S-1), dense tensors,
- *  N*H*W*C < 2^31 and N*P*Q*K < 2^31; else IGC_ERR_UNSUPPORTED.
+ *  Supported: C a multiple of 8 (16-byte pixel rows), strides 1..8, padding
+ *  with pad - (filter - 1) in [-128, 127] (the TMA im2col box corners), dense
+ *  tensors, N*H*W*C < 2^31 and N*P*Q*K < 2^31; else IGC_ERR_UNSUPPORTED.
+ *  When C is not a multiple of 128 the weights must be finite (padded channels
+ *  meet the next tap's weights with a zero input).
  *  N == 0 is a no-op.  Accuracy as for gemm_f16 with the sum over the taps.
  */
 int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R, int S,
@@ -270,6 +272,44 @@ int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R, int S,
                              const void *x, const void *w,
                              void *y, float *y_f32_check,
                              igc_stream_t stream);
+
+/*
+ * conv2d_nhwc_s8_zp -- INT8 convolution as an implicit GEMM with input zero
+ * points and requantisation: the pages' im2col lowering of the convolution
+ * ([P1] §2.2) applied to the INT8 path ([P1] §2.3), with [P3]'s padded input.
+ *
+ *   y32[n,p,q,k] = sum_{r<R} sum_{s<S} sum_{c<C}
+ *                  (xpad(n, p*stride_h + r - pad_h, q*stride_w + s - pad_w, c) - zX)
+ *                  * (w[k,r,s,c] - zW_k)                               (int32, wraps)
+ *   y8[n,p,q,k]  = clamp(rne(fp32(y32) * scale_k), -128, 127)
+ *
+ *  xpad is x inside [0,H) x [0,W) and zX outside: with asymmetric quantisation
+ *  the input's real zero is its zero point, so padded taps contribute nothing.
+ *  x       device NHWC bytes, uint8 (x_signed = 0) or int8 (x_signed = 1), dense.
+ *  zX      per-tensor zero point of x; must be a value of x's type.
+ *  w       device KRSC bytes, uint8 or int8 (w_signed), dense.
+ *  zW / zW_k  per-tensor zero point of w, or device int32[K] per output channel.
+ *  y32, y8 device NPQK int32 / int8 outputs (at least one non-NULL), dense.
+ *  scale / scale_k  per-tensor fp32 scale, or device float[K] per output channel.
+ *  workspace  device scratch of conv2d_nhwc_s8_zp_workspace_size(...) bytes,
+ *          256-byte aligned, caller-owned: the padded, shifted input (fp16),
+ *          the shifted weights (fp16) and the sums of both.
+ *  Rounding and exactness as for gemm_s8_zp (bit-exact).  Supported: C a
+ *  multiple of 8, strides 1..8, R, S <= 32, R*S*C < 2^24, x and w 16-byte
+ *  aligned; N == 0 is a no-op.
+ */
+int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S,
+                      int pad_h, int pad_w, int stride_h, int stride_w,
+                      const void *x, int x_signed, int32_t zX,
+                      const void *w, int w_signed, int32_t zW, const int32_t *zW_k,
+                      int32_t *y32, int8_t *y8,
+                      float scale, const float *scale_k,
+                      void *workspace, size_t workspace_bytes,
+                      igc_stream_t stream);
+
+/* Bytes of workspace conv2d_nhwc_s8_zp needs (0 if the shape is invalid or unsupported). */
+size_t conv2d_nhwc_s8_zp_workspace_size(int N, int H, int W, int C, int K, int R, int S,
+                                        int pad_h, int pad_w, int stride_h, int stride_w);
 
 /* Static description of a status code (never NULL). */
 const char *igc_status_string(int status);

@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_dequant.restype = ctypes.c_float
             L.oracle_dequant_matrix.argtypes = [i64, i64, vp, vp, vp, vp, vp]
             L.oracle_dequant_matrix.restype = None
+            L.oracle_conv2d_nhwc_s8_zp.argtypes = [i32] * 11 + [vp, i32, ctypes.c_int32, vp, i32,
+                                                                ctypes.c_int32, vp, vp, vp,
+                                                                ctypes.c_float, vp, i32]
+            L.oracle_conv2d_nhwc_s8_zp.restype = i32
             L.oracle_i32_to_f32_rne.argtypes = [ctypes.c_int32]
             L.oracle_i32_to_f32_rne.restype = ctypes.c_float
             L.oracle_requant.argtypes = [ctypes.c_int32, ctypes.c_float]
@@ -238,3 +242,29 @@ def fp16_accept(gpu: np.ndarray, ref: np.ndarray, sabs: np.ndarray, rel: float =
                          np.where(err > 0, np.inf, 0.0))
     ok = bool(np.all(np.isfinite(gpu)) and np.all(err <= bound))
     return ok, float(np.max(ratio)) if ratio.size else 0.0
+
+
+def conv2d_nhwc_s8_zp(x: np.ndarray, w: np.ndarray, *, x_signed: int, w_signed: int, zX: int,
+                      zW: int = 0, zW_k=None, pad=(1, 1), stride=(1, 1), scale: float = 0.0,
+                      scale_k=None, want_y8: bool = True, nthreads: int = 0):
+    """Direct int8 convolution with zero points (padding = zX): returns (y32, y8 or None, overflow)."""
+    x = np.ascontiguousarray(x).view(np.uint8)
+    w = np.ascontiguousarray(w).view(np.uint8)
+    N, H, W, C = x.shape
+    K, R, S, C2 = w.shape
+    assert C == C2
+    P = conv_out_dim(H, R, pad[0], stride[0])
+    Q = conv_out_dim(W, S, pad[1], stride[1])
+    if P <= 0 or Q <= 0:
+        raise ValueError("window does not fit")
+    zW_k = None if zW_k is None else np.ascontiguousarray(zW_k, dtype=np.int32)
+    scale_k = None if scale_k is None else np.ascontiguousarray(scale_k, dtype=np.float32)
+    y32 = np.empty((N, P, Q, K), np.int32)
+    y8 = np.empty((N, P, Q, K), np.int8) if want_y8 else None
+    rc = lib().oracle_conv2d_nhwc_s8_zp(N, H, W, C, K, R, S, pad[0], pad[1], stride[0], stride[1],
+                                        _ptr(x), int(x_signed), int(zX), _ptr(w), int(w_signed),
+                                        int(zW), _ptr(zW_k), _ptr(y32), _ptr(y8), float(scale),
+                                        _ptr(scale_k), nthreads)
+    if rc < 0:
+        raise ValueError("oracle_conv2d_nhwc_s8_zp: bad arguments")
+    return y32, y8, bool(rc == 1)

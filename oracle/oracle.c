@@ -546,3 +546,81 @@ int oracle_conv2d_nhwc_f16(int N, int H, int W, int C, int K, int R, int S,
     free(wd);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* INT8 convolution with zero points ([P1] §2.2-2.3 with [P3]'s padding):      */
+/*   y32[n,p,q,k] = sum_{r,s,c} (xpad - zX) * (w[k,r,s,c] - zW_k)              */
+/* xpad = x inside the image and zX outside, so a padded tap adds nothing.     */
+/* ------------------------------------------------------------------------ */
+
+struct conv_s8_ctx {
+    int N, H, W, C, K, R, S, ph, pw, sh, sw, P, Q;
+    const uint8_t *x;
+    int x_signed;
+    int32_t zX;
+    const uint8_t *w;
+    int w_signed;
+    int32_t zW;
+    const int32_t *zW_k;
+    int32_t *y32;
+    int8_t *y8;
+    float scale;
+    const float *scale_k;
+    volatile int overflow;
+};
+
+static void conv_s8_row(void *p, int64_t m)
+{
+    struct conv_s8_ctx *c = (struct conv_s8_ctx *)p;
+    int64_t pq = (int64_t)c->P * c->Q;
+    int n = (int)(m / pq);
+    int pp = (int)((m % pq) / c->Q);
+    int q = (int)(m % c->Q);
+    for (int k = 0; k < c->K; ++k) {
+        int64_t zw = c->zW_k ? c->zW_k[k] : c->zW;
+        int64_t s = 0;
+        for (int r = 0; r < c->R; ++r) {
+            int h = pp * c->sh + r - c->ph;
+            if (h < 0 || h >= c->H)
+                continue;                             /* padded tap: (zX - zX) * (...) = 0 */
+            for (int ss = 0; ss < c->S; ++ss) {
+                int w = q * c->sw + ss - c->pw;
+                if (w < 0 || w >= c->W)
+                    continue;
+                const uint8_t *xv = c->x + (((int64_t)n * c->H + h) * c->W + w) * c->C;
+                const uint8_t *wv = c->w + (((int64_t)k * c->R + r) * c->S + ss) * c->C;
+                for (int ch = 0; ch < c->C; ++ch)
+                    s += (q_value(xv[ch], c->x_signed) - c->zX) * (q_value(wv[ch], c->w_signed) - zw);
+            }
+        }
+        if (s > INT32_MAX || s < INT32_MIN)
+            c->overflow = 1;
+        int32_t s32 = (int32_t)(uint32_t)(uint64_t)s;
+        if (c->y32)
+            c->y32[m * c->K + k] = s32;
+        if (c->y8)
+            c->y8[m * c->K + k] = oracle_requant(s32, c->scale_k ? c->scale_k[k] : c->scale);
+    }
+}
+
+/* x: N*H*W*C bytes; w: K*R*S*C bytes; y32 / y8: N*P*Q*K (optional).
+ * Returns 0, 1 if some exact result does not fit int32, or -1 on bad args. */
+int oracle_conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S,
+                             int pad_h, int pad_w, int stride_h, int stride_w,
+                             const uint8_t *x, int x_signed, int32_t zX,
+                             const uint8_t *w, int w_signed, int32_t zW, const int32_t *zW_k,
+                             int32_t *y32, int8_t *y8, float scale, const float *scale_k,
+                             int nthreads)
+{
+    if (N < 0 || H <= 0 || W <= 0 || C <= 0 || K <= 0 || R <= 0 || S <= 0 ||
+        pad_h < 0 || pad_w < 0)
+        return -1;
+    int P = oracle_conv_out_dim(H, R, pad_h, stride_h);
+    int Q = oracle_conv_out_dim(W, S, pad_w, stride_w);
+    if (P <= 0 || Q <= 0)
+        return -1;
+    struct conv_s8_ctx c = {N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q,
+                            x, x_signed, zX, w, w_signed, zW, zW_k, y32, y8, scale, scale_k, 0};
+    parallel_rows((int64_t)N * P * Q, nthreads, conv_s8_row, &c);
+    return c.overflow ? 1 : 0;
+}

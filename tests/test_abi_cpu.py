@@ -14,7 +14,8 @@ def test_library_loads_and_exports_every_declared_symbol():
     L = igc.lib()
     names = igc.declared_functions()
     expected = {"gemm_f16", "gemm_bf16", "gemm_s8_zp", "gemm_s8_zp_workspace_size", "gemm_s8_zp_prepare",
-                "gemm_s8_zp_run", "gemm_s8_zp_dequant", "gemm_s8_zp_noalloc", "conv2d_nhwc_f16_implicit",
+                "gemm_s8_zp_run", "gemm_s8_zp_dequant", "gemm_s8_zp_noalloc",
+                "conv2d_nhwc_s8_zp", "conv2d_nhwc_s8_zp_workspace_size", "conv2d_nhwc_f16_implicit",
                 "igc_status_string", "igc_check_device_status", "igc_last_device_status",
                 "igc_set_wait_limit_ns", "igc_debug_wait_timeout_probe", "igc_version"}
     assert expected <= set(names)
@@ -78,7 +79,12 @@ def test_host_validation_before_any_device_call():
     assert conv(1, 14, 14, 256, 512, 3, 3, 1, 1, 1, 1, dummy, dummy, None, None, None) == igc.IGC_ERR_INVALID_ARG
     assert conv(0, 14, 14, 256, 512, 3, 3, 1, 1, 1, 1, None, None, dummy, None, None) == igc.IGC_OK
     # stride and channel-count limits are reported as unsupported before any device call
-    assert conv(1, 14, 14, 256, 512, 3, 3, 1, 1, 2, 2, dummy, dummy, dummy, None, None) == igc.IGC_ERR_UNSUPPORTED
+    assert conv(1, 14, 14, 256, 512, 3, 3, 1, 1, 9, 9, dummy, dummy, dummy, None, None) == igc.IGC_ERR_UNSUPPORTED
+    # int8 convolution: the padding value must be a value of the input type
+    c8 = L.conv2d_nhwc_s8_zp
+    assert c8(1, 8, 8, 16, 16, 3, 3, 1, 1, 1, 1, dummy, 0, 300, dummy, 1, 0, None, dummy, None,
+              1.0, None, dummy, 1 << 30, None) == igc.IGC_ERR_INVALID_ARG
+    assert L.conv2d_nhwc_s8_zp_workspace_size(1, 8, 8, 12, 16, 3, 3, 1, 1, 1, 1) == 0
     assert conv(1, 14, 14, 12, 512, 3, 3, 1, 1, 1, 1, dummy, dummy, dummy, None, None) == igc.IGC_ERR_UNSUPPORTED
 
 

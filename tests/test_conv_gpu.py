@@ -90,5 +90,19 @@ def test_unsupported_stride_reports_status():
     x = torch.zeros((1, 8, 8, 16), dtype=torch.float16, device="cuda")
     w = torch.zeros((16, 3, 3, 16), dtype=torch.float16, device="cuda")
     with pytest.raises(igc.IGCError) as e:
-        igc.conv2d_nhwc_f16_implicit(x, w, pad=(1, 1), stride=(2, 2))
+        igc.conv2d_nhwc_f16_implicit(x, w, pad=(1, 1), stride=(9, 9))
     assert e.value.status == igc.IGC_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("N,H,W,C,K,R,S,pad,stride", [
+    (2, 14, 14, 64, 128, 3, 3, (1, 1), (2, 2)),
+    (2, 9, 11, 16, 48, 3, 3, (1, 0), (2, 1)),
+    (1, 15, 15, 32, 64, 5, 5, (2, 2), (3, 3)),
+])
+def test_conv_strided_parity(N, H, W, C, K, R, S, pad, stride):
+    x = synth.normal_f16(N * 77 + C, 6, (N, H, W, C))
+    w = synth.normal_f16(K * 77 + R, 7, (K, R, S, C), std=1.0 / np.sqrt(R * S * C))
+    y, y32 = _gpu(x, w, pad, stride)
+    ref, sabs = oracle.conv2d_nhwc_f16(x, w, pad=pad, stride=stride)
+    assert_fp16_bound(y32, ref, sabs, f"stride {stride}")
+    assert_f16_is_rne_of_f32(y, y32, "strided conv")

@@ -433,3 +433,69 @@ def test_dequant_closed_forms():
     got = oracle.dequant_matrix(C32, s_row, s_col, bias)
     exact = np.abs(want) < 2**24
     assert np.array_equal(got[exact].astype(np.float64), want[exact])
+
+
+# ---------------------------------------------------------------------------
+# int8 convolution with zero points (padding value = zX)
+# ---------------------------------------------------------------------------
+
+def test_conv_s8_constant_zero_point_input_gives_zero_everywhere():
+    # with zero padding the border outputs would be (0 - zX)(w - zW) != 0
+    x = np.full((2, 6, 7, 8), 37, np.uint8)
+    w = RNG.integers(-128, 128, size=(5, 3, 3, 8)).astype(np.int8)
+    y32, _, _ = oracle.conv2d_nhwc_s8_zp(x, w, x_signed=0, w_signed=1, zX=37, zW=3, pad=(1, 1),
+                                         want_y8=False)
+    assert not y32.any()
+
+
+def test_conv_s8_1x1_equals_int8_gemm():
+    x = RNG.integers(0, 256, size=(3, 5, 4, 24)).astype(np.uint8)
+    w = RNG.integers(-128, 128, size=(16, 1, 1, 24)).astype(np.int8)
+    zW_k = RNG.integers(-5, 5, size=16).astype(np.int32)
+    y32, _, _ = oracle.conv2d_nhwc_s8_zp(x, w, x_signed=0, w_signed=1, zX=121, zW_k=zW_k,
+                                         pad=(0, 0), want_y8=False)
+    g32, _, _, _ = oracle.gemm_s8_zp(x.reshape(-1, 24), w.reshape(16, 24), a_signed=0, b_signed=1,
+                                     zA=121, zB_col=zW_k, want_c8=False)
+    assert np.array_equal(y32.reshape(-1, 16), g32)
+
+
+@pytest.mark.parametrize("pad,stride", [((1, 1), (1, 1)), ((0, 2), (2, 1)), ((2, 1), (2, 2))])
+def test_conv_s8_brute_force_im2col_with_zero_point_padding(pad, stride):
+    x = RNG.integers(0, 256, size=(2, 6, 5, 8)).astype(np.uint8)
+    w = RNG.integers(0, 256, size=(12, 3, 3, 8)).astype(np.uint8)
+    zX, zW = 90, 140
+    y32, _, _ = oracle.conv2d_nhwc_s8_zp(x, w, x_signed=0, w_signed=0, zX=zX, zW=zW, pad=pad,
+                                         stride=stride, want_y8=False)
+    N, H, W, C = x.shape
+    xp = np.full((N, H + 2 * pad[0], W + 2 * pad[1], C), zX, np.int64)
+    xp[:, pad[0]:pad[0] + H, pad[1]:pad[1] + W, :] = x
+    P = (H + 2 * pad[0] - 3) // stride[0] + 1
+    Q = (W + 2 * pad[1] - 3) // stride[1] + 1
+    cols = np.stack([xp[:, p * stride[0]:p * stride[0] + 3, q * stride[1]:q * stride[1] + 3, :]
+                     for p in range(P) for q in range(Q)], axis=1).reshape(N * P * Q, -1)
+    want = (cols - zX) @ (w.astype(np.int64).reshape(12, -1) - zW).T
+    assert np.array_equal(y32.reshape(-1, 12).astype(np.int64), want)
+
+
+def test_conv_s8_vs_float64_library_conv_on_shifted_values():
+    x = RNG.integers(-128, 128, size=(2, 7, 9, 16)).astype(np.int8)
+    w = RNG.integers(-128, 128, size=(8, 3, 3, 16)).astype(np.int8)
+    zX, zW = -3, 5
+    y32, _, _ = oracle.conv2d_nhwc_s8_zp(x, w, x_signed=1, w_signed=1, zX=zX, zW=zW, pad=(1, 1),
+                                         want_y8=False)
+    xt = torch.from_numpy(x.astype(np.float64) - zX).permute(0, 3, 1, 2)
+    wt = torch.from_numpy(w.astype(np.float64) - zW).permute(0, 3, 1, 2)
+    want = torch.nn.functional.conv2d(xt, wt, padding=1).permute(0, 2, 3, 1).numpy()
+    assert np.array_equal(y32.astype(np.float64), want)
+
+
+def test_conv_s8_delta_kernel_and_requant():
+    x = RNG.integers(0, 256, size=(1, 5, 6, 8)).astype(np.uint8)
+    zW = 7
+    w = np.full((8, 3, 3, 8), zW, np.int8)
+    w[np.arange(8), 1, 1, np.arange(8)] += 1                 # w - zW = delta at the centre tap
+    y32, y8, _ = oracle.conv2d_nhwc_s8_zp(x, w, x_signed=0, w_signed=1, zX=100, zW=zW,
+                                          pad=(1, 1), scale=0.5)
+    assert np.array_equal(y32, x.astype(np.int32) - 100)
+    assert np.array_equal(y8, np.array([[oracle.requant(int(v), 0.5) for v in row]
+                                        for row in y32.reshape(-1, 8)], np.int8).reshape(y8.shape))
