@@ -217,6 +217,103 @@ def e2e_measure(step: "Step", w3, w4, w5, steps: int):
     return ms, h2d, d2h
 
 
+def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
+    """Rows beyond the step (not part of `value`): each timed alone with CUDA events,
+    L2 flushed before every iteration, median of `iters`."""
+    import torch
+    import implicit_gemm_conv_tcgen05_gb300 as igc
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def t_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(iters):
+            flush.zero_()
+            s.record()
+            fn()
+            e.record()
+            e.synchronize()
+            ts.append(s.elapsed_time(e))
+        return float(np.median(ts))
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    out = {}
+    # bf16 GEMM 4096^3, bf16 out
+    A = t(synth.normal_bf16_bits(41, 1, (4096, 4096)).view(np.int16)).view(torch.bfloat16)
+    B = t(synth.normal_bf16_bits(41, 2, (4096, 4096)).view(np.int16)).view(torch.bfloat16)
+    C = torch.empty((4096, 4096), dtype=torch.bfloat16, device=device)
+    ms = t_ms(lambda: igc.gemm_bf16(A, B, C))
+    out["gemm_bf16_4096^3"] = {"ms": ms, "tflops": 2 * 4096 ** 3 / ms / 1e9}
+    del A, B, C
+    # int8 GEMM 8192^3 with the dequantised fp32 output (dequantise + bias fused)
+    w5 = synth.workload(5)
+    Aq, Bq = t(w5["A"]), t(w5["Bt"])
+    zA = t(w5["zA_row"])
+    srow = t(synth.uniform_f32(42, 1, (8192,), 1e-3, 1e-2))
+    scol = t(w5["scale_col"])
+    bias = t(synth.uniform_f32(42, 2, (8192,), -1.0, 1.0))
+    Y = torch.empty((8192, 8192), dtype=torch.float32, device=device)
+    ws = torch.empty(igc.gemm_s8_zp_workspace_size(8192, 8192, 8192), dtype=torch.uint8,
+                     device=device)
+    ms = t_ms(lambda: igc.gemm_s8_zp_dequant(Aq, Bq, zA_row=zA, scale_row=srow, scale_col=scol,
+                                             bias=bias, Y=Y, workspace=ws))
+    out["gemm_s8_zp_dequant_8192^3_f32_out"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
+    del Aq, Bq, Y, ws
+    # int8 convolution on the layer shape: x uint8 NHWC 256x14x14x256, w int8 512x3x3x256
+    x8 = t(synth.uniform_int(43, 6, (256, 14, 14, 256), 0, 255, np.uint8))
+    w8 = t(synth.uniform_int(43, 7, (512, 3, 3, 256), -127, 127, np.int8))
+    y8 = torch.empty((256, 14, 14, 512), dtype=torch.int8, device=device)
+    sk = t(synth.uniform_f32(43, 5, (512,), 1e-4, 1e-3))
+    wsc = torch.empty(igc.conv2d_nhwc_s8_zp_workspace_size(256, 14, 14, 256, 512, 3, 3),
+                      dtype=torch.uint8, device=device)
+    ms = t_ms(lambda: igc.conv2d_nhwc_s8_zp(x8, w8, 128, y8=y8, scale_k=sk, workspace=wsc))
+    out["conv3x3_s8_256x14x14x256->512"] = {"ms": ms,
+                                            "tops": OPS["conv3x3_256x14x14x256_512"] / ms / 1e9}
+    del x8, w8, y8, wsc
+    # stride-2 fp16 convolution: 256x28x28x128 -> 256, 3x3, pad 1 (P = Q = 14)
+    xs = t(synth.normal_f16(44, 6, (256, 28, 28, 128)))
+    wsx = t(synth.normal_f16(44, 7, (256, 3, 3, 128), std=1 / 34.0))
+    ys = torch.empty((256, 14, 14, 256), dtype=torch.float16, device=device)
+    ms = t_ms(lambda: igc.conv2d_nhwc_f16_implicit(xs, wsx, ys, pad=(1, 1), stride=(2, 2)))
+    out["conv3x3_stride2_256x28x28x128->256"] = {
+        "ms": ms, "tflops": 2.0 * 256 * 14 * 14 * 256 * 9 * 128 / ms / 1e9}
+    del xs, wsx, ys
+    # skinny fp16 GEMMs: M x 8192 x 8192 (B dominates the bytes)
+    Bk = t(synth.normal_f16(45, 2, (8192, 8192)))
+    for M in (512, 1024, 2048):
+        Am = t(synth.normal_f16(45 + M, 1, (M, 8192)))
+        Cm = torch.empty((M, 8192), dtype=torch.float16, device=device)
+        ms = t_ms(lambda: igc.gemm_f16(Am, Bk, Cm))
+        byts = 2.0 * (M * 8192 + 8192 * 8192 + M * 8192)
+        out[f"gemm_f16_{M}x8192x8192"] = {"ms": ms, "tflops": 2.0 * M * 8192 * 8192 / ms / 1e9,
+                                          "gbs": byts / ms / 1e6,
+                                          "hbm_frac": byts / ms / 1e6 / hbm_gbs if hbm_gbs else None}
+    del Bk
+    # the two small configurations: latency-bound
+    w1 = synth.workload(1)
+    A1, B1 = t(w1["A"]), t(w1["Bt"])
+    C1 = torch.empty((256, 256), dtype=torch.float32, device=device)
+    ms = t_ms(lambda: igc.gemm_f16(A1, B1, C1))
+    out["gemm_f16_256^3_f32_out"] = {"ms": ms, "tflops": 2 * 256 ** 3 / ms / 1e9,
+                                     "gbs": (2 * 2 * 256 * 256 + 4 * 256 * 256) / ms / 1e6}
+    w2 = synth.workload(2)
+    A2, B2 = t(w2["A"]), t(w2["Bt"])
+    C32 = torch.empty((1024, 1024), dtype=torch.int32, device=device)
+    C8 = torch.empty((1024, 1024), dtype=torch.int8, device=device)
+    ws2 = torch.empty(igc.gemm_s8_zp_workspace_size(1024, 1024, 1024), dtype=torch.uint8,
+                      device=device)
+    ms = t_ms(lambda: igc.gemm_s8_zp(A2, B2, zA=128, zB=121, C32=C32, C8=C8,
+                                     scale=w2["scale"], workspace=ws2))
+    out["gemm_s8_zp_1024^3_c32_c8"] = {"ms": ms, "tops": 2 * 1024 ** 3 / ms / 1e9,
+                                       "gbs": (2 * 1024 * 1024 + 5 * 1024 * 1024) / ms / 1e6}
+    for v in out.values():
+        tp = v.get("tflops", v.get("tops"))
+        v["frac_of_peak"] = tp / peak_tflops
+    return out
+
+
 def traffic_for(kernel_key: str):
     """DRAM bytes per launch of `kernel_key` from the committed ncu summary, if the
     kernel sources have not changed since it was taken."""
@@ -325,6 +422,11 @@ def run_ours(args, rank, world, local_rank):
                          "ms_per_step": e_ms, "steps": e2e_steps,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    if not args.no_extras:
+        result["extras"] = extras_measure(device, peak_burst, hbm)
+        result["extras_note"] = ("rows beyond the step, each timed alone (L2 flushed, median of "
+                                 "10); not part of value")
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w3, w4, w5, target_s=args.cpu_seconds)
     return result
@@ -407,6 +509,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
