@@ -73,6 +73,9 @@ extern "C" int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R
   p.out_f32 = y_f32_check;
   p.ldo32 = K;
   p.vec_ok = vec_store_ok(y, K, 2) && vec_store_ok(y_f32_check, K, 4);
-  return launch_auto_bn<Mode::ConvF16>(dev, tmA, w, Kg, K, static_cast<uint64_t>(Kg) * 2, p,
+  OutMaps om;
+  add_out_map(om, 0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, y, K, M, K, 2);
+  add_out_map(om, 1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y_f32_check, K, M, K, 4);
+  return launch_auto_bn<Mode::ConvF16>(dev, tmA, w, Kg, K, static_cast<uint64_t>(Kg) * 2, om, p,
                                        stream);
 }

@@ -47,5 +47,10 @@ extern "C" int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   p.out_f32 = C_f32_check;
   p.ldo32 = ldc32;
   p.vec_ok = vec_store_ok(C, ldc, esize) && vec_store_ok(C_f32_check, ldc32, 4);
-  return launch_auto_bn<Mode::GemmF16>(dev, tmA, Bt, K, N, ldb * 2, p, stream);
+  OutMaps om;
+  add_out_map(om, 0, c_dtype == IGC_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+              C, ldc, M, N, esize);
+  add_out_map(om, 1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C_f32_check, ldc32, M, N, 4);
+  return launch_auto_bn<Mode::GemmF16>(dev, tmA, Bt, K, N, ldb * 2, om, p, stream);
 }

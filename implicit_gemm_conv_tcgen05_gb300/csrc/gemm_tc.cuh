@@ -63,16 +63,20 @@ constexpr int kEpiWarps = 8;
 // Three warpgroups: warps 0-3 (TMA producer, MMA issuer / TMEM owner, two idle)
 // and two epilogue warpgroups (warps 4-11).  After set-up the first warpgroup
 // gives registers to the epilogue ones (setmaxnreg): kRegsLow + 2 kRegsHigh
-// warpgroup shares = 56 * 128 + 200 * 256 = 58368 registers, which fits the
+// warpgroup shares = 56 * 128 + 216 * 256 = 62464 registers, which fits the
 // launch's 384 threads x kMinLaunchRegs (checked on the host before launch).
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // 384
 constexpr int kRegsLow = 56;
-constexpr int kRegsHigh = 200;
-constexpr int kMinLaunchRegs = 152;
+constexpr int kRegsHigh = 216;
+constexpr int kMinLaunchRegs = 168;
 static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kThreads * kMinLaunchRegs, "register split");
 constexpr uint32_t kAtomABytes = BM_CTA * BK * 2;   // 16 KB
 constexpr uint32_t kStageABytes = kAtomABytes * kAtoms;
 constexpr uint32_t kBarrierBytes = 512;
+// Each epilogue warp stages 32 rows x 128 bytes of output in shared memory (128-byte
+// swizzle, the layout of a TMA box) and writes them with one bulk tensor store.
+constexpr uint32_t kStagingWarpBytes = 32 * 128;
+constexpr uint32_t kStagingBytes = kEpiWarps * kStagingWarpBytes;
 constexpr size_t kSmemBudget = 227 * 1024;
 constexpr int kIntChunkKb = 256 / KS;  // stages per exact fp32 chunk (256 k)
 
@@ -84,10 +88,11 @@ struct TileCfg {
   static constexpr uint32_t kStageBBytes = kAtomBBytes * kAtoms;
   static constexpr uint32_t kStageBytes = kStageABytes + kStageBBytes;
   static constexpr int kStages =
-      static_cast<int>((kSmemBudget - 1024 - kBarrierBytes) / kStageBytes) > 8
+      static_cast<int>((kSmemBudget - 1024 - kBarrierBytes - kStagingBytes) / kStageBytes) > 8
           ? 8
-          : static_cast<int>((kSmemBudget - 1024 - kBarrierBytes) / kStageBytes);
-  static constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes;
+          : static_cast<int>((kSmemBudget - 1024 - kBarrierBytes - kStagingBytes) / kStageBytes);
+  static constexpr size_t kSmemBytes =
+      1024 + kStages * kStageBytes + kStagingBytes + kBarrierBytes;
   static constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256 : 512;  // power of two >= 2*BN
   static constexpr int kEpiCols = BN / 2;  // columns per epilogue warp
 };
@@ -129,6 +134,10 @@ struct KParams {
   int32_t oA, oB;
   float scale;
   const float* scale_col;
+  int side_vec_ok;  // every non-null per-column vector is 16-byte aligned (vector loads)
+  // bit i set: output i is written by TMA stores through tensor map tmO<i>
+  // (float modes: 0 = out, 1 = out_f32; integer modes: 0 = c32, 1 = c8, 2 = yf)
+  int tma_out;
   // dequantised float output of the int8 path: y = ((fp32(C32) * dq_row_i) * dq_col_j) + bias_j
   float* yf;
   long long ldyf;
@@ -207,117 +216,302 @@ __device__ __forceinline__ void store_row_f32(float* out, long long ldo, int N, 
   }
 }
 
-// Row m of the tile, columns n0 .. n0+NC-1, values v (fp32 bit patterns).
+// One epilogue warp's staging buffer: lane l owns row l (128 bytes) of a 32-row
+// TMA box; 16-byte chunk k of the row sits at chunk k ^ (l % 8) (128-byte swizzle).
+struct Stager {
+  uint8_t* buf;  // 4 KB, 1024-byte aligned
+  int lane;
+  int row0;      // output row of lane 0
+  int M, N;      // output extent (a box wholly outside it is not issued)
+
+  // the previous store from this buffer must have read it before it is rewritten
+  __device__ __forceinline__ void begin() const {
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+  }
+  __device__ __forceinline__ void put(int k, uint4 v) const {
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) = v;
+  }
+  __device__ __forceinline__ void issue(const CUtensorMap* map, int col0) const {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < M && col0 < N) {
+      tma_store_2d(map, buf, col0, row0);
+      bulk_commit_group();
+    }
+  }
+};
+
+// 32-bit values (fp32 / int32 bit patterns), boxes of 32 columns.
 template <int NC>
-__device__ __forceinline__ void store_row_float(const KParams& p, int m, int n0,
+__device__ __forceinline__ void stage_store_u32(const Stager& st, const CUtensorMap* map, int n0,
                                                 const uint32_t (&v)[NC]) {
-  if (m >= p.M) return;
+#pragma unroll
+  for (int b = 0; b < NC / 32; ++b) {
+    st.begin();
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      st.put(k, make_uint4(v[b * 32 + 4 * k], v[b * 32 + 4 * k + 1], v[b * 32 + 4 * k + 2],
+                           v[b * 32 + 4 * k + 3]));
+    st.issue(map, n0 + b * 32);
+  }
+}
+
+// fp32 values rounded to fp16 / bf16, boxes of 64 columns.
+template <int NC, bool kBf16>
+__device__ __forceinline__ void stage_store_16bit(const Stager& st, const CUtensorMap* map, int n0,
+                                                  const uint32_t (&v)[NC]) {
+#pragma unroll
+  for (int b = 0; b < NC / 64; ++b) {
+    st.begin();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = b * 64 + 8 * k;
+      st.put(k, make_uint4(pack2<kBf16>(v[c], v[c + 1]), pack2<kBf16>(v[c + 2], v[c + 3]),
+                           pack2<kBf16>(v[c + 4], v[c + 5]), pack2<kBf16>(v[c + 6], v[c + 7])));
+    }
+    st.issue(map, n0 + b * 64);
+  }
+}
+
+// Row m of the tile, columns n0 .. n0+NC-1, values v (fp32 bit patterns).  Every
+// lane of the warp must call it (the TMA path is warp-collective); rows past M
+// are clipped by the store.
+template <int NC>
+__device__ __forceinline__ void store_row_float(const KParams& p, const CUtensorMap& tmO0,
+                                                const CUtensorMap& tmO1, const Stager& st, int m,
+                                                int n0, const uint32_t (&v)[NC]) {
   const bool full = p.vec_ok && (n0 + NC <= p.N);
   if (p.out != nullptr) {
-    if (p.out_type == kOutF16)
-      store_row_16bit<NC, false>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
-    else if (p.out_type == kOutBF16)
-      store_row_16bit<NC, true>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
-    else
-      store_row_f32<NC>(reinterpret_cast<float*>(p.out), p.ldo, p.N, m, n0, full, v);
+    if (p.tma_out & 1) {
+      if (p.out_type == kOutF16)
+        stage_store_16bit<NC, false>(st, &tmO0, n0, v);
+      else if (p.out_type == kOutBF16)
+        stage_store_16bit<NC, true>(st, &tmO0, n0, v);
+      else
+        stage_store_u32<NC>(st, &tmO0, n0, v);
+    } else if (m < p.M) {
+      if (p.out_type == kOutF16)
+        store_row_16bit<NC, false>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
+      else if (p.out_type == kOutBF16)
+        store_row_16bit<NC, true>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
+      else
+        store_row_f32<NC>(reinterpret_cast<float*>(p.out), p.ldo, p.N, m, n0, full, v);
+    }
   }
-  if (p.out_f32 != nullptr) store_row_f32<NC>(p.out_f32, p.ldo32, p.N, m, n0, full, v);
+  if (p.out_f32 != nullptr) {
+    if (p.tma_out & 2)
+      stage_store_u32<NC>(st, &tmO1, n0, v);
+    else if (m < p.M)
+      store_row_f32<NC>(p.out_f32, p.ldo32, p.N, m, n0, full, v);
+  }
 }
 
-__device__ __forceinline__ int8_t requant_i8(int32_t c, float s) {
-  // fp32(c) rounded to nearest even, one fp32 multiply, round half to even, clamp.
-  const float f = __fmul_rn(__int2float_rn(c), s);
-  int q = __float2int_rn(f);  // NaN -> 0, +-inf saturate
-  q = max(-128, min(127, q));
-  return static_cast<int8_t>(q);
+// Requantisation of one int32 result: fp32(c) rounded to nearest even, one fp32
+// multiply, clamp to [-128, 127] (a NaN product gives 0), then round half to
+// even by adding 1.5*2^23 (exact for |f| <= 2^22: the sum's ulp is 1, so the
+// fp32 add rounds f to the nearest integer, ties to even).  Returns the byte.
+__device__ __forceinline__ uint32_t requant_byte(int32_t c, float s) {
+  float f = __fmul_rn(__int2float_rn(c), s);
+  f = (f == f) ? fminf(fmaxf(f, -128.0f), 127.0f) : 0.0f;
+  return static_cast<uint32_t>(__float_as_int(__fadd_rn(f, 12582912.0f)) - 0x4B400000) & 0xFFu;
 }
 
-// sum[] holds, per column, n_chunks * 0x4B400000 + sum_k A'B' (mod 2^32).
+// kG consecutive entries of a per-column vector starting at column n: 16-byte
+// loads when allowed, else clamped scalar loads (tail of the matrix).
+constexpr int kG = 16;  // columns per step of the integer epilogue
+
+template <typename T>
+__device__ __forceinline__ void load_cols(const T* base, int n, int N, bool vec, T (&v)[kG]) {
+  static_assert(sizeof(T) == 4, "32-bit vectors");
+  if (vec) {
+#pragma unroll
+    for (int i = 0; i < kG / 4; ++i) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(base + n) + i);
+      reinterpret_cast<uint32_t*>(v)[4 * i + 0] = q.x;
+      reinterpret_cast<uint32_t*>(v)[4 * i + 1] = q.y;
+      reinterpret_cast<uint32_t*>(v)[4 * i + 2] = q.z;
+      reinterpret_cast<uint32_t*>(v)[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kG; ++i) v[i] = __ldg(base + (n + i < N ? n + i : N - 1));
+  }
+}
+
+// Per-row terms of the zero-point expansion, evaluated as
+//   C32 = S' - zB'_j (rA'_i - K zA'_i) - zA'_i cB'_j          (int32, mod 2^32)
+// which equals S' - zB'_j rA'_i - zA'_i cB'_j + K zA'_i zB'_j.
+struct IntRow {
+  uint32_t bias;       // n_chunks * 0x4B400000 carried by the running sums
+  uint32_t zAp;        // zA'_i
+  uint32_t u;          // rA'_i - K zA'_i
+  uint32_t t_uniform;  // zB' u + bias when zB is per tensor
+  float sA;            // dequantisation row scale
+  bool side_vec;       // per-column vectors may be read with 16-byte loads
+};
+
+__device__ __forceinline__ IntRow int_row(const KParams& p, int m, int n0, int NC, int n_chunks) {
+  const int mm = m < p.M ? m : p.M - 1;  // rows past M are computed (and clipped) like row M-1
+  IntRow r;
+  r.bias = static_cast<uint32_t>(n_chunks) * 0x4B400000u;
+  r.zAp = static_cast<uint32_t>((p.zA_row ? __ldg(p.zA_row + mm) : p.zA) - p.oA);
+  r.u = static_cast<uint32_t>(__ldg(p.rsumA + mm)) - static_cast<uint32_t>(p.K) * r.zAp;
+  r.t_uniform = static_cast<uint32_t>(p.zB - p.oB) * r.u + r.bias;
+  r.sA = p.dq_row ? __ldg(p.dq_row + mm) : 1.0f;
+  r.side_vec = (n0 + NC <= p.N) && p.side_vec_ok;
+  return r;
+}
+
+// C32 of the kG columns of group j (columns n0 + j kG ...).
 template <int NC>
-__device__ __forceinline__ void store_row_int(const KParams& p, int m, int n0,
+__device__ __forceinline__ void int_group(const KParams& p, const IntRow& r,
+                                          const uint32_t (&sum)[NC], int n0, int j,
+                                          int32_t (&c)[kG]) {
+  const int nj = n0 + j * kG;
+  int32_t cB[kG];
+  load_cols(p.csumB, nj, p.N, r.side_vec, cB);
+  if (p.zB_col) {
+    int32_t zB[kG];
+    load_cols(p.zB_col, nj, p.N, r.side_vec, zB);
+#pragma unroll
+    for (int i = 0; i < kG; ++i)
+      c[i] = static_cast<int32_t>(
+          sum[j * kG + i] - r.bias -
+          (static_cast<uint32_t>(zB[i]) - static_cast<uint32_t>(p.oB)) * r.u -
+          r.zAp * static_cast<uint32_t>(cB[i]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < kG; ++i)
+      c[i] = static_cast<int32_t>(sum[j * kG + i] - r.t_uniform -
+                                  r.zAp * static_cast<uint32_t>(cB[i]));
+  }
+}
+
+// The four requantised bytes of columns 4i .. 4i+3 of c, packed little-endian.
+__device__ __forceinline__ void int8_group(const KParams& p, const IntRow& r, int nj,
+                                           const int32_t (&c)[kG], uint32_t (&w)[kG / 4]) {
+  float sc[kG];
+  if (p.scale_col) {
+    load_cols(p.scale_col, nj, p.N, r.side_vec, sc);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kG; ++i) sc[i] = p.scale;
+  }
+#pragma unroll
+  for (int i = 0; i < kG / 4; ++i)
+    w[i] = requant_byte(c[4 * i], sc[4 * i]) | (requant_byte(c[4 * i + 1], sc[4 * i + 1]) << 8) |
+           (requant_byte(c[4 * i + 2], sc[4 * i + 2]) << 16) |
+           (requant_byte(c[4 * i + 3], sc[4 * i + 3]) << 24);
+}
+
+// Dequantised fp32 values of c: one RNE fp32 operation per step, in this order, no FMA.
+__device__ __forceinline__ void float_group(const KParams& p, const IntRow& r, int nj,
+                                            const int32_t (&c)[kG], uint32_t (&y)[kG]) {
+  float dcol[kG], bcol[kG];
+  if (p.dq_col) load_cols(p.dq_col, nj, p.N, r.side_vec, dcol);
+  if (p.bias) load_cols(p.bias, nj, p.N, r.side_vec, bcol);
+#pragma unroll
+  for (int i = 0; i < kG; ++i) {
+    float t = __int2float_rn(c[i]);
+    if (p.dq_row) t = __fmul_rn(t, r.sA);
+    if (p.dq_col) t = __fmul_rn(t, dcol[i]);
+    if (p.bias) t = __fadd_rn(t, bcol[i]);
+    y[i] = __float_as_uint(t);
+  }
+}
+
+// sum[] holds, per column, n_chunks * 0x4B400000 + sum_k A'B' (mod 2^32).  Writes
+// the requested integer-mode outputs of row m, columns n0 .. n0+NC-1.  Every lane
+// of the warp must call it (the TMA paths are warp-collective).
+template <int NC>
+__device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMap& tmO0,
+                                              const CUtensorMap& tmO1, const CUtensorMap& tmO2,
+                                              const Stager& st, int m, int n0,
                                               const uint32_t (&sum)[NC], int n_chunks) {
-  if (m >= p.M) return;
-  const uint32_t bias = static_cast<uint32_t>(n_chunks) * 0x4B400000u;
-  const uint32_t rA = static_cast<uint32_t>(p.rsumA[m]);
-  const uint32_t zAp = static_cast<uint32_t>((p.zA_row ? __ldg(p.zA_row + m) : p.zA) - p.oA);
-  const uint32_t Ku = static_cast<uint32_t>(p.K);
+  const IntRow r = int_row(p, m, n0, NC, n_chunks);
+  const bool in_row = m < p.M;
   const bool full = p.vec_ok && (n0 + NC <= p.N);
-  int32_t* row32 = p.c32 ? p.c32 + static_cast<size_t>(m) * p.ldc32 + n0 : nullptr;
-  int8_t* row8 = p.c8 ? p.c8 + static_cast<size_t>(m) * p.ldc8 + n0 : nullptr;
-  float* rowf = p.yf ? p.yf + static_cast<size_t>(m) * p.ldyf + n0 : nullptr;
-  const float sA = p.dq_row ? __ldg(p.dq_row + m) : 1.0f;
+  // int8 (requantised)
+  if (p.c8) {
+    if constexpr (NC >= 128) {
+      if (p.tma_out & 2) {
 #pragma unroll
-  for (int j = 0; j < NC / 16; ++j) {
-    int32_t c[16];
+        for (int b = 0; b < NC / 128; ++b) {
+          st.begin();
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int n = n0 + j * 16 + i;
-      const int nn = n < p.N ? n : p.N - 1;  // keep the side loads in bounds on the tail
-      const uint32_t zBp =
-          static_cast<uint32_t>((p.zB_col ? __ldg(p.zB_col + nn) : p.zB) - p.oB);
-      const uint32_t cB = static_cast<uint32_t>(__ldg(p.csumB + nn));
-      const uint32_t v = sum[j * 16 + i] - bias - zBp * rA - zAp * cB + Ku * zAp * zBp;
-      c[i] = static_cast<int32_t>(v);
-    }
-    if (row32) {
-      if (full) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          reinterpret_cast<int4*>(row32 + j * 16)[i] =
-              make_int4(c[4 * i], c[4 * i + 1], c[4 * i + 2], c[4 * i + 3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (n0 + j * 16 + i < p.N) row32[j * 16 + i] = c[i];
-      }
-    }
-    if (rowf) {
-      // dequantise: one RNE fp32 operation per step, in this order, no FMA
-      float y[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int n = n0 + j * 16 + i;
-        const int nn = n < p.N ? n : p.N - 1;
-        float t = __int2float_rn(c[i]);
-        if (p.dq_row) t = __fmul_rn(t, sA);
-        if (p.dq_col) t = __fmul_rn(t, __ldg(p.dq_col + nn));
-        if (p.bias) t = __fadd_rn(t, __ldg(p.bias + nn));
-        y[i] = t;
-      }
-      if (full) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          reinterpret_cast<float4*>(rowf + j * 16)[i] =
-              make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (n0 + j * 16 + i < p.N) rowf[j * 16 + i] = y[i];
-      }
-    }
-    if (row8) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t packed = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int n = n0 + j * 16 + 4 * i + b;
-          const int nn = n < p.N ? n : p.N - 1;
-          const float s = p.scale_col ? __ldg(p.scale_col + nn) : p.scale;
-          packed |= static_cast<uint32_t>(static_cast<uint8_t>(requant_i8(c[4 * i + b], s)))
-                    << (8 * b);
+          for (int g = 0; g < 128 / kG; ++g) {
+            int32_t c[kG];
+            uint32_t w[kG / 4];
+            int_group(p, r, sum, n0, b * (128 / kG) + g, c);
+            int8_group(p, r, n0 + (b * (128 / kG) + g) * kG, c, w);
+            st.put(g, make_uint4(w[0], w[1], w[2], w[3]));
+          }
+          st.issue(&tmO1, n0 + b * 128);
         }
-        w[i] = packed;
       }
-      if (full) {
-        reinterpret_cast<uint4*>(row8)[j] = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {
+    }
+    if (!(NC >= 128 && (p.tma_out & 2)) && in_row) {
+      int8_t* row8 = p.c8 + static_cast<size_t>(m) * p.ldc8 + n0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (n0 + j * 16 + i < p.N)
-            row8[j * 16 + i] = static_cast<int8_t>((w[i / 4] >> (8 * (i % 4))) & 0xFFu);
+      for (int j = 0; j < NC / kG; ++j) {
+        int32_t c[kG];
+        uint32_t w[kG / 4];
+        int_group(p, r, sum, n0, j, c);
+        int8_group(p, r, n0 + j * kG, c, w);
+        if (full) {
+          reinterpret_cast<uint4*>(row8)[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kG; ++i)
+            if (n0 + j * kG + i < p.N)
+              row8[j * kG + i] = static_cast<int8_t>((w[i / 4] >> (8 * (i % 4))) & 0xFFu);
+        }
       }
+    }
+  }
+  // int32 and dequantised fp32: 32-bit values, boxes of 32 columns (two groups)
+#pragma unroll
+  for (int o = 0; o < 2; ++o) {
+    void* outp = o == 0 ? static_cast<void*>(p.c32) : static_cast<void*>(p.yf);
+    if (outp == nullptr) continue;
+    const bool tma = (p.tma_out >> (o == 0 ? 0 : 2)) & 1;
+    const CUtensorMap* map = o == 0 ? &tmO0 : &tmO2;
+    const long long ld = o == 0 ? p.ldc32 : p.ldyf;
+    uint32_t* row = reinterpret_cast<uint32_t*>(outp) + static_cast<size_t>(in_row ? m : 0) * ld + n0;
+#pragma unroll
+    for (int b = 0; b < NC / 32; ++b) {
+      if (tma) st.begin();
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int j = 2 * b + g;
+        int32_t c[kG];
+        uint32_t y[kG];
+        int_group(p, r, sum, n0, j, c);
+        if (o == 0) {
+#pragma unroll
+          for (int i = 0; i < kG; ++i) y[i] = static_cast<uint32_t>(c[i]);
+        } else {
+          float_group(p, r, n0 + j * kG, c, y);
+        }
+        if (tma) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st.put(g * 4 + i, make_uint4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]));
+        } else if (in_row) {
+          if (full) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              reinterpret_cast<uint4*>(row + j * kG)[i] =
+                  make_uint4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kG; ++i)
+              if (n0 + j * kG + i < p.N) row[j * kG + i] = y[i];
+          }
+        }
+      }
+      if (tma) st.issue(map, n0 + b * 32);
     }
   }
 }
@@ -342,25 +536,21 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&v)[NC]
 }
 
 // Adds the exact integers held in NC fp32 TMEM columns to the running sums
-// (bits of x + 1.5*2^23, i.e. 0x4B400000 + x for |x| <= 2^22): 32 columns per load.
+// (bits of x + 1.5*2^23, i.e. 0x4B400000 + x for |x| <= 2^22): two 32-column loads per wait.
 template <int NC>
 __device__ __forceinline__ void tmem_drain_add(uint32_t taddr, uint32_t (&sum)[NC]) {
+  static_assert(NC % 64 == 0, "drain in steps of 64 columns");
 #pragma unroll
-  for (int j = 0; j < NC / 32; ++j) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr + j * 32, r);
+  for (int j = 0; j < NC / 64; ++j) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_32x32b_x32(taddr + j * 64, r0);
+    tmem_ld_32x32b_x32(taddr + j * 64 + 32, r1);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      sum[j * 32 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r[i]), 12582912.0f));
-  }
-  if constexpr (NC % 32 != 0) {
-    uint32_t r[16];
-    tmem_ld_32x32b_x16(taddr + (NC / 32) * 32, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      sum[(NC / 32) * 32 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r[i]), 12582912.0f));
+    for (int i = 0; i < 32; ++i) {
+      sum[j * 64 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r0[i]), 12582912.0f));
+      sum[j * 64 + 32 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r1[i]), 12582912.0f));
+    }
   }
 }
 
@@ -370,7 +560,10 @@ __device__ __forceinline__ void tmem_drain_add(uint32_t taddr, uint32_t (&sum)[N
 template <Mode kMode, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     igc_tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const KParams p) {
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmO0,
+                       const __grid_constant__ CUtensorMap tmO1,
+                       const __grid_constant__ CUtensorMap tmO2, const KParams p) {
   using Cfg = TileCfg<BN>;
   constexpr int kStages = Cfg::kStages;
   constexpr int NC = Cfg::kEpiCols;
@@ -381,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * Cfg::kStageBBytes);
+  uint8_t* staging = sB + kStages * Cfg::kStageBBytes;  // 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
   uint64_t* full = bars;                 // leader: both CTAs' copies of stage s landed
   uint64_t* empty = bars + kStages;      // each CTA: stage s may be overwritten
   uint64_t* tfull = bars + 2 * kStages;  // each CTA: accumulator a is ready
@@ -588,6 +782,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(half * NC);
     const int n_chunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
+    Stager st;
+    st.buf = staging + ew * kStagingWarpBytes;
+    st.lane = lane;
+    st.M = p.M;
+    st.N = p.N;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = cluster; t < p.num_tiles; t += num_clusters) {
@@ -595,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(p, t, mb, nb);
       const int m = mb * BM + static_cast<int>(rank) * BM_CTA + row_in_cta;
       const int n0 = nb * BN + half * NC;
+      st.row0 = m - lane;
       if constexpr (!mode_is_int(kMode)) {
         if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag,
                                                         p.status, kSiteEpiFull)))
@@ -608,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
-        store_row_float<NC>(p, m, n0, v);
+        store_row_float<NC>(p, tmO0, tmO1, st, m, n0, v);
       } else {
         uint32_t sum[NC];
 #pragma unroll
@@ -625,10 +825,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
-        store_row_int<NC>(p, m, n0, sum, n_chunks);
+        store_row_int<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum, n_chunks);
       }
     }
-  epi_done:;
+  epi_done:
+    // every staged store of this warp has completed before the CTA may exit
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
     }
   }
 

@@ -10,6 +10,10 @@
 
 namespace igc {
 
+inline bool vec_store_ok(const void* p, long long ld, size_t esize) {
+  return p == nullptr || (aligned16(p) && (static_cast<unsigned long long>(ld) * esize) % 16 == 0);
+}
+
 template <Mode kMode, int BN>
 struct KernelSlot {
   std::once_flag once[64];
@@ -70,9 +74,29 @@ int kernel_setup(const DeviceInfo& dev, int* max_clusters) {
   return s.rc[d];
 }
 
+// Tensor maps of the outputs written by bulk tensor stores from the epilogue's
+// staging buffers; bit i of mask enables map i (the others are never read).
+struct OutMaps {
+  CUtensorMap map[3] = {};
+  int mask = 0;
+};
+
+// Enables output slot `slot` (an M x N row-major matrix, row stride ld elements
+// of esize bytes) for bulk tensor stores when its base and row stride are
+// 16-byte aligned; boxes are 32 rows x 128 bytes, 128-byte swizzled.  Otherwise
+// the slot stays on direct stores.
+inline void add_out_map(OutMaps& o, int slot, CUtensorMapDataType dtype, const void* ptr,
+                        long long ld, long long M, long long N, size_t esize) {
+  if (ptr == nullptr || !vec_store_ok(ptr, ld, esize)) return;
+  if (encode_tiled_2d(&o.map[slot], dtype, ptr, static_cast<uint64_t>(N),
+                      static_cast<uint64_t>(M), static_cast<uint64_t>(ld) * esize,
+                      static_cast<uint32_t>(128 / esize), 32) == IGC_OK)
+    o.mask |= 1 << slot;
+}
+
 template <Mode kMode, int BN>
 int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                   KParams p, cudaStream_t stream) {
+                   const OutMaps& om, KParams p, cudaStream_t stream) {
   int max_clusters = 0;
   int rc = kernel_setup<kMode, BN>(dev, &max_clusters);
   if (rc != IGC_OK) return rc;
@@ -84,6 +108,7 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;  // m-tiles walked together (measured best of 2-16)
   p.wait_limit_ns = wait_limit_ns();
   p.status = status_word();
+  p.tma_out = om.mask;
   const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
 
   cudaLaunchConfig_t cfg = {};
@@ -98,7 +123,8 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN>, tmA, tmB, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN>, tmA, tmB, om.map[0],
+                         om.map[1], om.map[2], p) != cudaSuccess) {
     (void)cudaGetLastError();
     return IGC_ERR_CUDA;
   }
@@ -135,8 +161,8 @@ constexpr int kNumBn = sizeof(kBnCands) / sizeof(kBnCands[0]);
 // BN/2 rows (each CTA of the pair loads half of the B tile) and launches.
 template <Mode kMode>
 int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_base,
-                   uint64_t b_inner, uint64_t b_rows, uint64_t b_row_bytes, KParams p,
-                   cudaStream_t stream) {
+                   uint64_t b_inner, uint64_t b_rows, uint64_t b_row_bytes, const OutMaps& om,
+                   KParams p, cudaStream_t stream) {
   constexpr CUtensorMapDataType kBType = kMode == Mode::GemmBF16
                                              ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -149,8 +175,8 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
                        b_row_bytes, BK, static_cast<uint32_t>(bn / 2));
   if (rc != IGC_OK) return rc;
   switch (bn) {
-    case 256: return launch_tc_gemm<kMode, 256>(dev, tmA, tmB, p, stream);
-    case 128: return launch_tc_gemm<kMode, 128>(dev, tmA, tmB, p, stream);
+    case 256: return launch_tc_gemm<kMode, 256>(dev, tmA, tmB, om, p, stream);
+    case 128: return launch_tc_gemm<kMode, 128>(dev, tmA, tmB, om, p, stream);
     default: return IGC_ERR_UNSUPPORTED;
   }
 }
@@ -164,10 +190,6 @@ inline int zero_rows(void* ptr, long long ld, long long rows, long long cols, si
                            stream) == cudaSuccess
              ? IGC_OK
              : IGC_ERR_CUDA;
-}
-
-inline bool vec_store_ok(const void* p, long long ld, size_t esize) {
-  return p == nullptr || (aligned16(p) && (static_cast<unsigned long long>(ld) * esize) % 16 == 0);
 }
 
 }  // namespace igc
