@@ -258,10 +258,6 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
   p.scale = scale;
   p.scale_col = scale_k;
   p.vec_ok = vec_store_ok(y32, K, 4) && vec_store_ok(y8, K, 1);
-  p.side_vec_ok = aligned16(p.csumB) && (p.zB_col == nullptr || aligned16(p.zB_col)) &&
-                  (p.scale_col == nullptr || aligned16(p.scale_col)) &&
-                  (p.dq_col == nullptr || aligned16(p.dq_col)) &&
-                  (p.bias == nullptr || aligned16(p.bias));
   OutMaps om;
   add_out_map(om, 0, CU_TENSOR_MAP_DATA_TYPE_INT32, y32, K, c.M, K, 4);
   add_out_map(om, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, y8, K, c.M, K, 1);

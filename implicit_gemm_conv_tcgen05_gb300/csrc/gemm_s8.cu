@@ -175,10 +175,6 @@ int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, in
   p.bias = dq.bias;
   p.vec_ok = vec_store_ok(C32, ldc32, 4) && vec_store_ok(C8, ldc8, 1) &&
              vec_store_ok(dq.y, dq.ldy, 4);
-  p.side_vec_ok = aligned16(p.csumB) && (p.zB_col == nullptr || aligned16(p.zB_col)) &&
-                  (p.scale_col == nullptr || aligned16(p.scale_col)) &&
-                  (p.dq_col == nullptr || aligned16(p.dq_col)) &&
-                  (p.bias == nullptr || aligned16(p.bias));
   OutMaps om;
   add_out_map(om, 0, CU_TENSOR_MAP_DATA_TYPE_INT32, C32, ldc32, M, N, 4);
   add_out_map(om, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, C8, ldc8, M, N, 1);

@@ -112,6 +112,9 @@ struct KParams {
   int num_kb;
   int tiles_m, tiles_n, num_tiles;
   int group_m;
+  // persistent schedule: tiles before tail_start are whole work units; every
+  // tile from tail_start on is split into two column halves (num_units in all)
+  int tail_start, num_units;
   int chunk_kb;
   int conv_P, conv_Q, conv_cblocks, conv_S, conv_C;
   int pad_h, pad_w, stride_h, stride_w;
@@ -134,7 +137,6 @@ struct KParams {
   int32_t oA, oB;
   float scale;
   const float* scale_col;
-  int side_vec_ok;  // every non-null per-column vector is 16-byte aligned (vector loads)
   // bit i set: output i is written by TMA stores through tensor map tmO<i>
   // (float modes: 0 = out, 1 = out_f32; integer modes: 0 = c32, 1 = c8, 2 = yf)
   int tma_out;
@@ -156,6 +158,30 @@ __device__ __forceinline__ void tile_coords(const KParams& p, int t, int& mb, in
   const int r = t - g * per_group;
   mb = first_m + r % gm;
   nb = r / gm;
+}
+
+// Work unit u: a whole BM x BN tile, or (u past tail_start) one BM x BN/2 column
+// half j of a tile.  The halves fill the schedule's last round with twice as
+// many units of half the length.
+struct Unit {
+  int mb, nb;
+  int j;      // column half (0 for a whole tile)
+  bool half;  // the unit covers BN/2 columns starting at nb*BN + j*BN/2
+};
+
+__device__ __forceinline__ Unit unit_coords(const KParams& p, int u) {
+  Unit w;
+  int t = u;
+  w.j = 0;
+  w.half = false;
+  if (u >= p.tail_start) {
+    const int v = u - p.tail_start;
+    t = p.tail_start + (v >> 1);
+    w.j = v & 1;
+    w.half = true;
+  }
+  tile_coords(p, t, w.mb, w.nb);
+  return w;
 }
 
 // ---------------------------------------------------------------------------
@@ -317,26 +343,44 @@ __device__ __forceinline__ uint32_t requant_byte(int32_t c, float s) {
   return static_cast<uint32_t>(__float_as_int(__fadd_rn(f, 12582912.0f)) - 0x4B400000) & 0xFFu;
 }
 
-// kG consecutive entries of a per-column vector starting at column n: 16-byte
-// loads when allowed, else clamped scalar loads (tail of the matrix).
 constexpr int kG = 16;  // columns per step of the integer epilogue
 
-template <typename T>
-__device__ __forceinline__ void load_cols(const T* base, int n, int N, bool vec, T (&v)[kG]) {
-  static_assert(sizeof(T) == 4, "32-bit vectors");
-  if (vec) {
+// The per-column vectors of one warp's NC columns, spread over its lanes: lane l
+// holds column n0 + 32 b + l in element b.  They are read with one coalesced
+// load per 32 columns, all issued together, and a column's value is broadcast
+// to the warp by a shuffle where it is used.  Columns past N read column N-1
+// (their outputs are never stored); absent vectors read as 0.
+template <int NC>
+struct ColVecs {
+  static constexpr int kB = (NC + 31) / 32;
+  uint32_t cB[kB], zB[kB], sc[kB], dq[kB], bi[kB];
+};
+
+template <int NB>
+__device__ __forceinline__ void load_col_vec(const void* base, int n0, int N, int lane,
+                                             uint32_t (&v)[NB]) {
+  const uint32_t* b32 = static_cast<const uint32_t*>(base);
 #pragma unroll
-    for (int i = 0; i < kG / 4; ++i) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(base + n) + i);
-      reinterpret_cast<uint32_t*>(v)[4 * i + 0] = q.x;
-      reinterpret_cast<uint32_t*>(v)[4 * i + 1] = q.y;
-      reinterpret_cast<uint32_t*>(v)[4 * i + 2] = q.z;
-      reinterpret_cast<uint32_t*>(v)[4 * i + 3] = q.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < kG; ++i) v[i] = __ldg(base + (n + i < N ? n + i : N - 1));
+  for (int b = 0; b < NB; ++b) {
+    const int n = n0 + 32 * b + lane;
+    v[b] = b32 ? __ldg(b32 + (n < N ? n : N - 1)) : 0u;
   }
+}
+
+template <int NC>
+__device__ __forceinline__ void load_col_vecs(const KParams& p, int n0, int lane,
+                                              ColVecs<NC>& V) {
+  load_col_vec(p.csumB, n0, p.N, lane, V.cB);
+  load_col_vec(p.zB_col, n0, p.N, lane, V.zB);
+  load_col_vec(p.scale_col, n0, p.N, lane, V.sc);
+  load_col_vec(p.dq_col, n0, p.N, lane, V.dq);
+  load_col_vec(p.bias, n0, p.N, lane, V.bi);
+}
+
+// Column c (0 .. NC-1, a constant after unrolling) of a lane-spread vector.
+template <int NB>
+__device__ __forceinline__ uint32_t col_val(const uint32_t (&v)[NB], int c) {
+  return __shfl_sync(0xffffffffu, v[c >> 5], c & 31);
 }
 
 // Per-row terms of the zero-point expansion, evaluated as
@@ -348,10 +392,9 @@ struct IntRow {
   uint32_t u;          // rA'_i - K zA'_i
   uint32_t t_uniform;  // zB' u + bias when zB is per tensor
   float sA;            // dequantisation row scale
-  bool side_vec;       // per-column vectors may be read with 16-byte loads
 };
 
-__device__ __forceinline__ IntRow int_row(const KParams& p, int m, int n0, int NC, int n_chunks) {
+__device__ __forceinline__ IntRow int_row(const KParams& p, int m, int n_chunks) {
   const int mm = m < p.M ? m : p.M - 1;  // rows past M are computed (and clipped) like row M-1
   IntRow r;
   r.bias = static_cast<uint32_t>(n_chunks) * 0x4B400000u;
@@ -359,45 +402,35 @@ __device__ __forceinline__ IntRow int_row(const KParams& p, int m, int n0, int N
   r.u = static_cast<uint32_t>(__ldg(p.rsumA + mm)) - static_cast<uint32_t>(p.K) * r.zAp;
   r.t_uniform = static_cast<uint32_t>(p.zB - p.oB) * r.u + r.bias;
   r.sA = p.dq_row ? __ldg(p.dq_row + mm) : 1.0f;
-  r.side_vec = (n0 + NC <= p.N) && p.side_vec_ok;
   return r;
 }
 
-// C32 of the kG columns of group j (columns n0 + j kG ...).
+// C32 of the kG columns of group j (tile columns j kG ...).
 template <int NC>
-__device__ __forceinline__ void int_group(const KParams& p, const IntRow& r,
-                                          const uint32_t (&sum)[NC], int n0, int j,
-                                          int32_t (&c)[kG]) {
-  const int nj = n0 + j * kG;
-  int32_t cB[kG];
-  load_cols(p.csumB, nj, p.N, r.side_vec, cB);
+__device__ __forceinline__ void int_group(const KParams& p, const IntRow& r, const ColVecs<NC>& V,
+                                          const uint32_t (&sum)[NC], int j, int32_t (&c)[kG]) {
   if (p.zB_col) {
-    int32_t zB[kG];
-    load_cols(p.zB_col, nj, p.N, r.side_vec, zB);
 #pragma unroll
     for (int i = 0; i < kG; ++i)
-      c[i] = static_cast<int32_t>(
-          sum[j * kG + i] - r.bias -
-          (static_cast<uint32_t>(zB[i]) - static_cast<uint32_t>(p.oB)) * r.u -
-          r.zAp * static_cast<uint32_t>(cB[i]));
+      c[i] = static_cast<int32_t>(sum[j * kG + i] - r.bias -
+                                  (col_val(V.zB, j * kG + i) - static_cast<uint32_t>(p.oB)) * r.u -
+                                  r.zAp * col_val(V.cB, j * kG + i));
   } else {
 #pragma unroll
     for (int i = 0; i < kG; ++i)
       c[i] = static_cast<int32_t>(sum[j * kG + i] - r.t_uniform -
-                                  r.zAp * static_cast<uint32_t>(cB[i]));
+                                  r.zAp * col_val(V.cB, j * kG + i));
   }
 }
 
 // The four requantised bytes of columns 4i .. 4i+3 of c, packed little-endian.
-__device__ __forceinline__ void int8_group(const KParams& p, const IntRow& r, int nj,
+template <int NC>
+__device__ __forceinline__ void int8_group(const KParams& p, const ColVecs<NC>& V, int j,
                                            const int32_t (&c)[kG], uint32_t (&w)[kG / 4]) {
   float sc[kG];
-  if (p.scale_col) {
-    load_cols(p.scale_col, nj, p.N, r.side_vec, sc);
-  } else {
 #pragma unroll
-    for (int i = 0; i < kG; ++i) sc[i] = p.scale;
-  }
+  for (int i = 0; i < kG; ++i)
+    sc[i] = p.scale_col ? __uint_as_float(col_val(V.sc, j * kG + i)) : p.scale;
 #pragma unroll
   for (int i = 0; i < kG / 4; ++i)
     w[i] = requant_byte(c[4 * i], sc[4 * i]) | (requant_byte(c[4 * i + 1], sc[4 * i + 1]) << 8) |
@@ -406,30 +439,33 @@ __device__ __forceinline__ void int8_group(const KParams& p, const IntRow& r, in
 }
 
 // Dequantised fp32 values of c: one RNE fp32 operation per step, in this order, no FMA.
-__device__ __forceinline__ void float_group(const KParams& p, const IntRow& r, int nj,
-                                            const int32_t (&c)[kG], uint32_t (&y)[kG]) {
-  float dcol[kG], bcol[kG];
-  if (p.dq_col) load_cols(p.dq_col, nj, p.N, r.side_vec, dcol);
-  if (p.bias) load_cols(p.bias, nj, p.N, r.side_vec, bcol);
+template <int NC>
+__device__ __forceinline__ void float_group(const KParams& p, const IntRow& r,
+                                            const ColVecs<NC>& V, int j, const int32_t (&c)[kG],
+                                            uint32_t (&y)[kG]) {
 #pragma unroll
   for (int i = 0; i < kG; ++i) {
     float t = __int2float_rn(c[i]);
     if (p.dq_row) t = __fmul_rn(t, r.sA);
-    if (p.dq_col) t = __fmul_rn(t, dcol[i]);
-    if (p.bias) t = __fadd_rn(t, bcol[i]);
+    if (p.dq_col) t = __fmul_rn(t, __uint_as_float(col_val(V.dq, j * kG + i)));
+    if (p.bias) t = __fadd_rn(t, __uint_as_float(col_val(V.bi, j * kG + i)));
     y[i] = __float_as_uint(t);
   }
 }
 
 // sum[] holds, per column, n_chunks * 0x4B400000 + sum_k A'B' (mod 2^32).  Writes
 // the requested integer-mode outputs of row m, columns n0 .. n0+NC-1.  Every lane
-// of the warp must call it (the TMA paths are warp-collective).
+// of the warp must call it and run every group: the column values are broadcast
+// by shuffles and the TMA paths are warp-collective; only the direct stores are
+// predicated on the row.
 template <int NC>
 __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMap& tmO0,
                                               const CUtensorMap& tmO1, const CUtensorMap& tmO2,
                                               const Stager& st, int m, int n0,
                                               const uint32_t (&sum)[NC], int n_chunks) {
-  const IntRow r = int_row(p, m, n0, NC, n_chunks);
+  const IntRow r = int_row(p, m, n_chunks);
+  ColVecs<NC> V;
+  load_col_vecs<NC>(p, n0, st.lane, V);
   const bool in_row = m < p.M;
   const bool full = p.vec_ok && (n0 + NC <= p.N);
   // int8 (requantised)
@@ -443,22 +479,25 @@ __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMa
           for (int g = 0; g < 128 / kG; ++g) {
             int32_t c[kG];
             uint32_t w[kG / 4];
-            int_group(p, r, sum, n0, b * (128 / kG) + g, c);
-            int8_group(p, r, n0 + (b * (128 / kG) + g) * kG, c, w);
+            int_group<NC>(p, r, V, sum, b * (128 / kG) + g, c);
+            int8_group<NC>(p, V, b * (128 / kG) + g, c, w);
             st.put(g, make_uint4(w[0], w[1], w[2], w[3]));
           }
           st.issue(&tmO1, n0 + b * 128);
         }
       }
     }
-    if (!(NC >= 128 && (p.tma_out & 2)) && in_row) {
-      int8_t* row8 = p.c8 + static_cast<size_t>(m) * p.ldc8 + n0;
+    if (!(NC >= 128 && (p.tma_out & 2))) {
+      // every lane computes (the column values are shuffled across the warp);
+      // rows past M store nothing
+      int8_t* row8 = p.c8 + static_cast<size_t>(in_row ? m : 0) * p.ldc8 + n0;
 #pragma unroll
       for (int j = 0; j < NC / kG; ++j) {
         int32_t c[kG];
         uint32_t w[kG / 4];
-        int_group(p, r, sum, n0, j, c);
-        int8_group(p, r, n0 + j * kG, c, w);
+        int_group<NC>(p, r, V, sum, j, c);
+        int8_group<NC>(p, V, j, c, w);
+        if (!in_row) continue;
         if (full) {
           reinterpret_cast<uint4*>(row8)[j] = make_uint4(w[0], w[1], w[2], w[3]);
         } else {
@@ -487,12 +526,12 @@ __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMa
         const int j = 2 * b + g;
         int32_t c[kG];
         uint32_t y[kG];
-        int_group(p, r, sum, n0, j, c);
+        int_group<NC>(p, r, V, sum, j, c);
         if (o == 0) {
 #pragma unroll
           for (int i = 0; i < kG; ++i) y[i] = static_cast<uint32_t>(c[i]);
         } else {
-          float_group(p, r, n0 + j * kG, c, y);
+          float_group<NC>(p, r, V, j, c, y);
         }
         if (tma) {
 #pragma unroll
@@ -633,11 +672,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
-    for (int t = cluster; t < p.num_tiles; t += num_clusters) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+    for (int u = cluster; u < p.num_units; u += num_clusters) {
+      const Unit w = unit_coords(p, u);
+      const int mb = w.mb;
       const int m_cta = mb * BM + static_cast<int>(rank) * BM_CTA;
-      const int n_cta = nb * BN + static_cast<int>(rank) * Cfg::kBNHalf;
+      // each CTA holds half of the unit's B rows at the start of its stage buffer
+      // (a half unit uses the first BN/4 of the BN/2 rows the box brings in)
+      const int n_cta = w.half ? w.nb * BN + w.j * (BN / 2) + static_cast<int>(rank) * (BN / 4)
+                               : w.nb * BN + static_cast<int>(rank) * Cfg::kBNHalf;
       int cn = 0, ch = 0, cw = 0;
       if constexpr (mode_is_conv(kMode)) {
         const int PQ = p.conv_P * p.conv_Q;
@@ -710,7 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (leader)
     // The whole warp runs the loop (converged); lane 0 issues MMAs and commits.
     if (rank == 0) {
-      constexpr uint32_t idesc = make_idesc_kind_f16(BM, BN, kMode == Mode::GemmBF16 ? 1u : 0u);
+      constexpr uint32_t idesc_full =
+          make_idesc_kind_f16(BM, BN, kMode == Mode::GemmBF16 ? 1u : 0u);
+      constexpr uint32_t idesc_half =
+          make_idesc_kind_f16(BM, BN / 2, kMode == Mode::GemmBF16 ? 1u : 0u);
       // descriptors of stage 0, atom 0, k 0; the start-address field (bits 0-13,
       // in 16-byte units) is advanced by adding offsets >> 4 (no carry: < 256 KB)
       const uint64_t adesc0 = make_sw128_kmajor_desc(smem_u32(sA));
@@ -719,7 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int t = cluster; t < p.num_tiles; t += num_clusters) {
+      for (int u = cluster; u < p.num_units; u += num_clusters) {
+        const uint32_t idesc = u >= p.tail_start ? idesc_half : idesc_full;
         int kin = 0;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (kin == 0) {
@@ -789,11 +835,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     st.N = p.N;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = cluster; t < p.num_tiles; t += num_clusters) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
-      const int m = mb * BM + static_cast<int>(rank) * BM_CTA + row_in_cta;
-      const int n0 = nb * BN + half * NC;
+    for (int u = cluster; u < p.num_units; u += num_clusters) {
+      const Unit w = unit_coords(p, u);
+      const int m = w.mb * BM + static_cast<int>(rank) * BM_CTA + row_in_cta;
+      // a half unit's NC columns are handled by the half-0 warps alone; the
+      // others only take part in the accumulator hand-offs
+      const bool active = !w.half || half == 0;
+      const int n0 = w.half ? w.nb * BN + w.j * NC : w.nb * BN + half * NC;
       st.row0 = m - lane;
       if constexpr (!mode_is_int(kMode)) {
         if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag,
@@ -801,14 +849,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           goto epi_done;
         tc_fence_after();
         uint32_t v[NC];
-        tmem_load_cols<NC>(lane_base + static_cast<uint32_t>(acc * BN), v);
-        tmem_ld_wait();
+        if (active) {
+          tmem_load_cols<NC>(lane_base + static_cast<uint32_t>(acc * BN), v);
+          tmem_ld_wait();
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
-        store_row_float<NC>(p, tmO0, tmO1, st, m, n0, v);
+        if (active) store_row_float<NC>(p, tmO0, tmO1, st, m, n0, v);
       } else {
         uint32_t sum[NC];
 #pragma unroll
@@ -818,14 +868,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                           p.status, kSiteEpiFull)))
             goto epi_done;
           tc_fence_after();
-          tmem_drain_add<NC>(lane_base + static_cast<uint32_t>(acc * BN), sum);
+          if (active) tmem_drain_add<NC>(lane_base + static_cast<uint32_t>(acc * BN), sum);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
-        store_row_int<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum, n_chunks);
+        if (active) store_row_int<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum, n_chunks);
       }
     }
   epi_done:

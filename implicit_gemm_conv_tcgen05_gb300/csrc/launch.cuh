@@ -103,13 +103,18 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   p.tiles_m = static_cast<int>((static_cast<long long>(p.M) + BM - 1) / BM);
   p.tiles_n = static_cast<int>((static_cast<long long>(p.N) + BN - 1) / BN);
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
-  if (tiles > 0x7fffffffLL) return IGC_ERR_UNSUPPORTED;
+  if (tiles > 0x7fff0000LL) return IGC_ERR_UNSUPPORTED;  // units (tiles + tail halves) fit an int
   p.num_tiles = static_cast<int>(tiles);
   p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;  // m-tiles walked together (measured best of 2-16)
+  // When the last round of the schedule would be at most half full, its tiles
+  // run as column halves: the round holds twice the units at half the length.
+  const int rem = p.num_tiles % max_clusters;
+  p.tail_start = (rem > 0 && 2 * rem <= max_clusters) ? p.num_tiles - rem : p.num_tiles;
+  p.num_units = p.num_tiles + (p.num_tiles - p.tail_start);
   p.wait_limit_ns = wait_limit_ns();
   p.status = status_word();
   p.tma_out = om.mask;
-  const int clusters = p.num_tiles < max_clusters ? p.num_tiles : max_clusters;
+  const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
@@ -132,8 +137,9 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
 }
 
 // Tile width for an M x N output: the candidate with the smallest estimated
-// time, (waves of tiles over the CTA pairs) x (tile width / relative efficiency
-// of that width); ties go to the wider tile.
+// time, (rounds of the schedule over the CTA pairs, a last round of column
+// halves counting one half) x (tile width / relative efficiency of that width);
+// ties go to the wider tile.
 inline int pick_bn(long long M, long long N, int clusters, const int* cands, const double* eff,
                    int n_cands) {
   const long long tm = (M + BM - 1) / BM;
@@ -141,8 +147,10 @@ inline int pick_bn(long long M, long long N, int clusters, const int* cands, con
   double best_cost = 1e300;
   for (int i = 0; i < n_cands; ++i) {
     const long long tiles = tm * ((N + cands[i] - 1) / cands[i]);
-    const long long waves = (tiles + clusters - 1) / clusters;
-    const double cost = static_cast<double>(waves) * cands[i] / eff[i];
+    const long long rem = tiles % clusters;
+    const double rounds = static_cast<double>(tiles / clusters) +
+                          (rem == 0 ? 0.0 : (2 * rem <= clusters ? 0.5 : 1.0));
+    const double cost = rounds * cands[i] / eff[i];
     if (cost < best_cost * 0.999) {
       best_cost = cost;
       best = cands[i];

@@ -121,3 +121,16 @@ def test_repeated_calls_are_deterministic():
     C1, _ = _run(A, Bt)
     C2, _ = _run(A, Bt)
     assert np.array_equal(C1, C2)
+
+
+@pytest.mark.parametrize("M,N,K", [(2560, 2048, 128), (2304, 2304, 64)])
+def test_whole_tiles_and_split_last_round_full_output(M, N, K):
+    """80 and 81 tiles of 256 x 256: more than one round of the persistent
+    schedule, with a short last round that runs as column halves.  Every
+    output is compared."""
+    A = synth.uniform_f16(M + 1, 1, (M, K))
+    Bt = synth.uniform_f16(N + 2, 2, (N, K))
+    C16, C32 = _run(A, Bt, torch.float16, with_check=True)
+    ref, sabs = oracle.gemm_f16(A, Bt)
+    assert_fp16_bound(C32, ref, sabs, f"{M}x{N}x{K} fp32")
+    assert_f16_is_rne_of_f32(C16, C32, f"{M}x{N}x{K}")

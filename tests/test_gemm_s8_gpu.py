@@ -150,3 +150,20 @@ def test_workspace_too_small_rejected():
         igc.gemm_s8_zp(A, Bt, C32=torch.empty((64, 64), dtype=torch.int32, device="cuda"),
                        workspace=ws)
     assert e.value.status == igc.IGC_ERR_WORKSPACE
+
+
+def test_whole_tiles_and_split_last_round_bit_exact():
+    """80 tiles of 256 x 256 (more than one round of the persistent schedule, a
+    short last round of column halves), per-row zA and per-column zB, every
+    output compared."""
+    rng = np.random.default_rng(80)
+    M, N, K = 2560, 2048, 320
+    A = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+    Bt = rng.integers(-128, 128, size=(N, K)).astype(np.int8)
+    kw = dict(zA_row=rng.integers(0, 256, size=M).astype(np.int32),
+              zB_col=rng.integers(-128, 128, size=N).astype(np.int32),
+              scale_col=synth.uniform_f32(80, 5, (N,), 1e-5, 1e-4))
+    g32, g8 = _gpu(A, Bt, **kw)
+    o32, o8, _ = _oracle(A, Bt, **kw)
+    _assert_equal(g32, o32, "C32")
+    _assert_equal(g8, o8, "C8")
