@@ -56,12 +56,42 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def csrc_digest() -> str:
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and blank-space differences (string
+    literals are kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def csrc_digest(sources: dict | None = None) -> str:
+    """Digest of the kernel sources' code (comments and spacing ignored): the key
+    under which ncu traffic figures stay valid."""
+    if sources is None:
+        sources = {}
+        for name in os.listdir(KERNEL_SOURCES):
+            if name.endswith((".cu", ".cuh", ".h")):
+                with open(os.path.join(KERNEL_SOURCES, name), encoding="utf-8") as f:
+                    sources[name] = f.read()
     h = hashlib.sha256()
-    for name in sorted(os.listdir(KERNEL_SOURCES)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(KERNEL_SOURCES, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(sources):
+        h.update(name.encode() + b"\0" + _code_only(sources[name]).encode())
     return h.hexdigest()[:16]
 
 

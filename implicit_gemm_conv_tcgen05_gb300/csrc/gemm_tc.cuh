@@ -12,26 +12,36 @@
 //   GemmInt : exact integer GEMM of int8 operands that were shifted to [-128, 127]
 //             and widened to fp16 by the pre-pass (every such value, and every
 //             product, is exact in fp16/fp32), with the zero-point correction and
-//             requantisation fused into the epilogue (page "TVM在CUDA GPU上跑GEMM
-//             的全套张量化实现", §2.3).
+//             requantisation (or dequantisation + bias) fused into the epilogue
+//             (page "TVM在CUDA GPU上跑GEMM的全套张量化实现", §2.3).
+//   GemmBF16: GemmF16 with bf16 operands (the same kind::f16 pipe, §3.3's
+//             "f16 -> bf16" swap).
+//   ConvInt : ConvF16's gather with GemmInt's arithmetic (int8 convolution over
+//             a zero-point-padded, shifted input).
 //
 // A cluster of two CTAs (on two SMs) computes one 256 x BN output tile with
 // tcgen05.mma.cta_group::2 (M = 256): CTA r holds rows [128 r, 128 r + 128) of
 // the A tile and rows [BN/2 r, BN/2 (r+1)) of the B tile in its own shared
 // memory, and receives its 128 x BN accumulator in its own tensor memory.
-// Warp roles in each CTA:
-//   warp 0      TMA producer (one lane): its CTA's halves of A and B into a
-//               multi-stage ring (128-byte swizzle); both CTAs' copies complete
-//               on the leader CTA's `full[s]` barrier.
-//   warp 1      tensor-memory owner; in the leader CTA also the MMA issuer (one
-//               lane): 4 x tcgen05.mma per 64-deep k-block, tcgen05.commit
-//               multicast to both CTAs frees ring stages (`empty[s]`) and hands
-//               finished accumulators to both epilogues (`tfull[a]`).
-//   warps 2..9  epilogue: tcgen05.ld of their lane quadrant / column half,
-//               fused output math, predicated global stores; they release an
-//               accumulator on the leader's `tempty[a]` (16 arrivals).
+// Warp roles in each CTA (384 threads, three warpgroups):
+//   warp 0      TMA producer: its CTA's halves of A and B into a ring of
+//               128-deep stages (two 128-byte swizzle atoms per operand); both
+//               CTAs' copies complete on the leader CTA's `full[s]` barrier.
+//   warp 1      tensor-memory owner; in the leader CTA also the MMA issuer: 8 x
+//               tcgen05.mma per stage, tcgen05.commit multicast to both CTAs frees
+//               ring stages (`empty[s]`) and hands finished accumulators to both
+//               epilogues (`tfull[a]`).  Warps 0 and 1 run their loops converged;
+//               lane 0 issues.
+//   warps 2-3   idle (their warpgroup gives registers to the epilogue).
+//   warps 4-11  epilogue: tcgen05.ld of their lane quadrant / column half, fused
+//               output math, outputs staged in 128-byte-swizzled shared memory and
+//               written by TMA bulk tensor stores (direct stores for outputs TMA
+//               cannot address); they release an accumulator on the leader's
+//               `tempty[a]` (16 arrivals).
 // Two accumulators (2 x BN of the 512 TMEM columns) let the epilogue of one
-// tile overlap the main loop of the next.
+// tile overlap the main loop of the next.  The persistent schedule walks tiles
+// in groups of 8 m-tiles; when its last round would fill at most half of the
+// CTA pairs, that round's tiles run as two BN/2-wide column halves.
 //
 // The integer modes accumulate in chunks that fp32 holds exactly: products of
 // the shifted operands are integers of magnitude <= 2^14, so a chunk of 256 k
