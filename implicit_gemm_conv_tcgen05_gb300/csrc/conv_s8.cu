@@ -123,6 +123,51 @@ static __global__ void __launch_bounds__(256) pad_shift_pixels_kernel(
   if (lane == 0) px[pixel] = acc;
 }
 
+// One thread per 16 channels of a padded pixel, for C = 16 G with G a power of
+// two <= 32, so the G threads of a pixel are an aligned group of lanes of one
+// warp: x' = x_q - oX inside the image (exact fp16 by the pre-pass's byte
+// widening), zX - oX in the border; lane 0 of the group writes the pixel's
+// channel sum.  Threads past the end still take part in the shuffles.
+static __global__ void __launch_bounds__(256) pad_shift_chunks_kernel(
+    const uint8_t* __restrict__ x, uint32_t flip, int border, int N, int H, int W, int C, int ph,
+    int pw, int Hp, int Wp, int log2g, __half* __restrict__ xp, int32_t* __restrict__ px) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long npix = static_cast<long long>(N) * Hp * Wp;
+  const bool valid = t < (npix << log2g);
+  const long long pixel = t >> log2g;
+  const int g = static_cast<int>(t & ((1 << log2g) - 1));
+  int32_t part = 0;
+  if (valid) {
+    const int n = static_cast<int>(pixel / (static_cast<long long>(Hp) * Wp));
+    const int rem = static_cast<int>(pixel - static_cast<long long>(n) * Hp * Wp);
+    const int h = rem / Wp - ph;
+    const int w = rem % Wp - pw;
+    uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(pixel) * C + g * 16);
+    if (h >= 0 && h < H && w >= 0 && w < W) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+          x + ((static_cast<size_t>(n) * H + h) * W + w) * C + g * 16));
+      uint32_t out[8];
+      uint32_t usum = 0;
+      widen4(raw.x, flip, out[0], out[1], usum);
+      widen4(raw.y, flip, out[2], out[3], usum);
+      widen4(raw.z, flip, out[4], out[5], usum);
+      widen4(raw.w, flip, out[6], out[7], usum);
+      dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+      dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+      part = static_cast<int32_t>(usum - 128u * 16u);
+    } else {
+      const uint32_t hb = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(border)));
+      const uint32_t bb = hb | (hb << 16);
+      dst[0] = make_uint4(bb, bb, bb, bb);
+      dst[1] = make_uint4(bb, bb, bb, bb);
+      part = 16 * border;
+    }
+  }
+  for (int off = (1 << log2g) >> 1; off > 0; off >>= 1)
+    part += __shfl_xor_sync(0xffffffffu, part, off);
+  if (valid && g == 0) px[pixel] = part;
+}
+
 // One thread per output pixel m = (n, p, q): rX'[m] = sum over the R x S window
 // (in padded coordinates, origin (p sh, q sw)) of the pixel sums.
 static __global__ void __launch_bounds__(256) window_sums_kernel(const int32_t* __restrict__ px, int N,
@@ -205,9 +250,19 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
   {
     const long long npix = c.N * c.Hp * c.Wp;
     const int vec = (C % 16 == 0) && aligned16(x);
-    pad_shift_pixels_kernel<<<static_cast<unsigned>((npix + 7) / 8), 256, 0, stream>>>(
-        static_cast<const uint8_t*>(x), x_signed ? 1 : 0, oX, zX - oX, N, H, W, C, pad_h, pad_w,
-        static_cast<int>(c.Hp), static_cast<int>(c.Wp), vec, xp, px);
+    const int groups = C / 16;
+    if (vec && groups <= 32 && (groups & (groups - 1)) == 0) {
+      int log2g = 0;
+      while ((1 << log2g) < groups) ++log2g;
+      const long long threads = npix << log2g;
+      pad_shift_chunks_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+          static_cast<const uint8_t*>(x), x_signed ? 0x80808080u : 0u, zX - oX, N, H, W, C,
+          pad_h, pad_w, static_cast<int>(c.Hp), static_cast<int>(c.Wp), log2g, xp, px);
+    } else {
+      pad_shift_pixels_kernel<<<static_cast<unsigned>((npix + 7) / 8), 256, 0, stream>>>(
+          static_cast<const uint8_t*>(x), x_signed ? 1 : 0, oX, zX - oX, N, H, W, C, pad_h,
+          pad_w, static_cast<int>(c.Hp), static_cast<int>(c.Wp), vec, xp, px);
+    }
     if (cudaGetLastError() != cudaSuccess) return IGC_ERR_CUDA;
   }
   // 2. weights: K rows of R*S*C values

@@ -36,6 +36,24 @@ static __device__ __forceinline__ int shifted_byte(uint32_t byte, int is_signed,
          offset;
 }
 
+// Four packed bytes to four exact fp16 values, two per 32-bit word (byte order
+// kept).  u = byte (uint8) or byte with its top bit flipped (int8: flip =
+// 0x80808080, so u = value + 128); placed in the low mantissa byte of 0x6400,
+// u reads as the fp16 number 1024 + u, and subtracting 1152 = 1024 + 128 leaves
+// u - 128 exactly (|u - 128| <= 128).  usum += the sum of the four u.
+static __device__ __forceinline__ void widen4(uint32_t word, uint32_t flip, uint32_t& lo,
+                                              uint32_t& hi, uint32_t& usum) {
+  const uint32_t u = word ^ flip;
+  usum = __dp4a(u, 0x01010101u, usum);
+  const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // (1024 + u0, 1024 + u1)
+  const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);  // (1024 + u2, 1024 + u3)
+  const __half2 k1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+  const __half2 ra = __hsub2(*reinterpret_cast<const __half2*>(&a), k1152);
+  const __half2 rb = __hsub2(*reinterpret_cast<const __half2*>(&b), k1152);
+  lo = *reinterpret_cast<const uint32_t*>(&ra);
+  hi = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
 // One warp per row: dst[row, k] = fp16(src[row, k] - offset) for k < K, 0 for
 // K <= k < Kp; sums[row] = sum_k (src[row, k] - offset).  Both operands of a
 // GEMM go through one launch.
@@ -61,6 +79,9 @@ static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const Pr
   const int K = pp.K;
   int32_t acc = 0;
   if (o.vec) {
+    // offset 128 (uint8) keeps the byte, offset 0 (int8) flips its top bit
+    const uint32_t flip = o.offset == 128 ? 0u : 0x80808080u;
+    uint32_t usum = 0;  // sum of the u bytes; the shifted sum is usum - 128 K
     for (int k0 = lane * 16; k0 < K; k0 += 32 * 16 * kPrepassUnroll) {
       uint4 raw[kPrepassUnroll];
 #pragma unroll
@@ -72,25 +93,18 @@ static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const Pr
       for (int u = 0; u < kPrepassUnroll; ++u) {
         const int k = k0 + u * 32 * 16;
         if (k >= K) break;
-        const uint32_t words[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
         uint32_t out[8];
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          int v[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            v[b] = shifted_byte((words[wi] >> (8 * b)) & 0xFFu, o.is_signed, o.offset);
-            acc += v[b];
-          }
-          __half2 h0 = __halves2half2(__int2half_rn(v[0]), __int2half_rn(v[1]));
-          __half2 h1 = __halves2half2(__int2half_rn(v[2]), __int2half_rn(v[3]));
-          out[2 * wi] = *reinterpret_cast<uint32_t*>(&h0);
-          out[2 * wi + 1] = *reinterpret_cast<uint32_t*>(&h1);
-        }
+        widen4(raw[u].x, flip, out[0], out[1], usum);
+        widen4(raw[u].y, flip, out[2], out[3], usum);
+        widen4(raw[u].z, flip, out[4], out[5], usum);
+        widen4(raw[u].w, flip, out[6], out[7], usum);
         reinterpret_cast<uint4*>(d + k)[0] = make_uint4(out[0], out[1], out[2], out[3]);
         reinterpret_cast<uint4*>(d + k)[1] = make_uint4(out[4], out[5], out[6], out[7]);
       }
     }
+    // the lane read 16 bytes at k = 16 lane + 512 i for every such k < K
+    const uint32_t nbytes = K > lane * 16 ? 16u * static_cast<uint32_t>((K - lane * 16 + 511) / 512) : 0u;
+    acc = static_cast<int32_t>(usum - 128u * nbytes);
   } else {
     for (int k = lane; k < pp.Kp; k += 32) {
       int v = 0;

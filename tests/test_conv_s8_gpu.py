@@ -28,6 +28,8 @@ def _data(N, H, W, C, K, R, S, x_signed, w_signed, seed):
     (1, 10, 12, 72, 200, 5, 3, (2, 1), (1, 2), (1, 0)),    # rectangular window, mixed strides
     (2, 8, 8, 32, 64, 1, 1, (0, 0), (1, 1), (0, 1)),       # 1x1
     (4, 6, 6, 128, 96, 3, 3, (0, 0), (1, 1), (0, 1)),      # no padding
+    (2, 6, 7, 64, 48, 3, 3, (1, 1), (1, 1), (1, 1)),       # int8 input, 4 chunks per pixel
+    (1, 5, 5, 512, 32, 3, 3, (1, 1), (1, 1), (1, 0)),      # int8 input, 32 chunks per pixel
 ])
 def test_conv_s8_parity(N, H, W, C, K, R, S, pad, stride, signs):
     x, w, rng = _data(N, H, W, C, K, R, S, *signs, seed=N * 100 + C + K)
