@@ -268,6 +268,29 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
             ts.append(s.elapsed_time(e))
         return float(np.median(ts))
 
+    def graph_ms(fn, n=100, reps=5):
+        """Per-call time of n calls captured in one CUDA graph (median of reps replays)."""
+        side = torch.cuda.Stream(device=device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(n):
+                    fn()
+        torch.cuda.current_stream().wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for _ in range(reps):
+            s.record()
+            g.replay()
+            e.record()
+            e.synchronize()
+            ts.append(s.elapsed_time(e) / n)
+        return float(np.median(ts))
+
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
     out = {}
     # bf16 GEMM 4096^3, bf16 out
@@ -338,6 +361,13 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
                                      scale=w2["scale"], workspace=ws2))
     out["gemm_s8_zp_1024^3_c32_c8"] = {"ms": ms, "tops": 2 * 1024 ** 3 / ms / 1e9,
                                        "gbs": (2 * 1024 * 1024 + 5 * 1024 * 1024) / ms / 1e6}
+    # the same two calls as 100 back-to-back launches replayed from a CUDA graph
+    # (no host launch cost; inputs stay in L2 between the launches)
+    ms = graph_ms(lambda: igc.gemm_f16(A1, B1, C1))
+    out["gemm_f16_256^3_f32_out_graph100"] = {"ms": ms, "tflops": 2 * 256 ** 3 / ms / 1e9}
+    ms = graph_ms(lambda: igc.gemm_s8_zp(A2, B2, zA=128, zB=121, C32=C32, C8=C8,
+                                         scale=w2["scale"], workspace=ws2))
+    out["gemm_s8_zp_1024^3_c32_c8_graph100"] = {"ms": ms, "tops": 2 * 1024 ** 3 / ms / 1e9}
     for v in out.values():
         tp = v.get("tflops", v.get("tops"))
         v["frac_of_peak"] = tp / peak_tflops
@@ -455,7 +485,8 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_extras:
         result["extras"] = extras_measure(device, peak_burst, hbm)
         result["extras_note"] = ("rows beyond the step, each timed alone (L2 flushed, median of "
-                                 "10); not part of value")
+                                 "10; *_graph100 rows: per-call time of 100 launches replayed "
+                                 "from a CUDA graph, L2 warm); not part of value")
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w3, w4, w5, target_s=args.cpu_seconds)

@@ -72,6 +72,8 @@ static __global__ void __launch_bounds__(256) pad_shift_pixels_kernel(
     const uint8_t* __restrict__ x, int is_signed, int offset, int border, int N, int H, int W,
     int C, int ph, int pw, int Hp, int Wp, int vec, __half* __restrict__ xp,
     int32_t* __restrict__ px) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const long long pixel = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = static_cast<int>(threadIdx.x % 32);
   const long long npix = static_cast<long long>(N) * Hp * Wp;
@@ -131,6 +133,8 @@ static __global__ void __launch_bounds__(256) pad_shift_pixels_kernel(
 static __global__ void __launch_bounds__(256) pad_shift_chunks_kernel(
     const uint8_t* __restrict__ x, uint32_t flip, int border, int N, int H, int W, int C, int ph,
     int pw, int Hp, int Wp, int log2g, __half* __restrict__ xp, int32_t* __restrict__ px) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long npix = static_cast<long long>(N) * Hp * Wp;
   const bool valid = t < (npix << log2g);
@@ -174,6 +178,8 @@ static __global__ void __launch_bounds__(256) window_sums_kernel(const int32_t* 
                                                           int Hp, int Wp, int P, int Q, int R,
                                                           int S, int sh, int sw,
                                                           int32_t* __restrict__ rx) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const long long m = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long M = static_cast<long long>(N) * P * Q;
   if (m >= M) return;
@@ -255,15 +261,17 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
       int log2g = 0;
       while ((1 << log2g) < groups) ++log2g;
       const long long threads = npix << log2g;
-      pad_shift_chunks_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-          static_cast<const uint8_t*>(x), x_signed ? 0x80808080u : 0u, zX - oX, N, H, W, C,
-          pad_h, pad_w, static_cast<int>(c.Hp), static_cast<int>(c.Wp), log2g, xp, px);
+      rc = launch_pdl(pad_shift_chunks_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)),
+                      dim3(256), 0, stream, static_cast<const uint8_t*>(x),
+                      x_signed ? 0x80808080u : 0u, zX - oX, N, H, W, C, pad_h, pad_w,
+                      static_cast<int>(c.Hp), static_cast<int>(c.Wp), log2g, xp, px);
     } else {
-      pad_shift_pixels_kernel<<<static_cast<unsigned>((npix + 7) / 8), 256, 0, stream>>>(
-          static_cast<const uint8_t*>(x), x_signed ? 1 : 0, oX, zX - oX, N, H, W, C, pad_h,
-          pad_w, static_cast<int>(c.Hp), static_cast<int>(c.Wp), vec, xp, px);
+      rc = launch_pdl(pad_shift_pixels_kernel, dim3(static_cast<unsigned>((npix + 7) / 8)),
+                      dim3(256), 0, stream, static_cast<const uint8_t*>(x), x_signed ? 1 : 0, oX,
+                      zX - oX, N, H, W, C, pad_h, pad_w, static_cast<int>(c.Hp),
+                      static_cast<int>(c.Wp), vec, xp, px);
     }
-    if (cudaGetLastError() != cudaSuccess) return IGC_ERR_CUDA;
+    if (rc != IGC_OK) return rc;
   }
   // 2. weights: K rows of R*S*C values
   {
@@ -272,10 +280,11 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
     if (rc != IGC_OK) return rc;
   }
   // 3. window sums of the im2col rows
-  window_sums_kernel<<<static_cast<unsigned>((c.M + 255) / 256), 256, 0, stream>>>(
-      px, N, static_cast<int>(c.Hp), static_cast<int>(c.Wp), static_cast<int>(c.P),
-      static_cast<int>(c.Q), R, S, stride_h, stride_w, rx);
-  if (cudaGetLastError() != cudaSuccess) return IGC_ERR_CUDA;
+  rc = launch_pdl(window_sums_kernel, dim3(static_cast<unsigned>((c.M + 255) / 256)), dim3(256),
+                  0, stream, static_cast<const int32_t*>(px), N, static_cast<int>(c.Hp),
+                  static_cast<int>(c.Wp), static_cast<int>(c.P), static_cast<int>(c.Q), R, S,
+                  stride_h, stride_w, rx);
+  if (rc != IGC_OK) return rc;
 
   // 4. the implicit GEMM over the padded tensor (no padding left for TMA)
   CUtensorMap tmA;

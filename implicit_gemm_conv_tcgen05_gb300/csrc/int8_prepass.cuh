@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 
 #include "igc_host.h"
+#include "sm100_ptx.cuh"
 
 namespace igc {
 namespace prepass {
@@ -58,6 +59,8 @@ static __device__ __forceinline__ void widen4(uint32_t word, uint32_t flip, uint
 // K <= k < Kp; sums[row] = sum_k (src[row, k] - offset).  Both operands of a
 // GEMM go through one launch.
 static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const PrepassParams pp) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
   const int lane = static_cast<int>(threadIdx.x % 32);
   // select the operand field by field (a dynamic index into the parameter
@@ -141,8 +144,8 @@ inline int launch_prepass(const PrepassOperand* ops, int n_ops, long long K, lon
   pp.Kp = static_cast<int>(Kp);
   const long long rows = static_cast<long long>(pp.op[0].rows) + (n_ops > 1 ? pp.op[1].rows : 0);
   const long long blocks = (rows + 7) / 8;
-  shift_widen_rowsum_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(pp);
-  return cudaGetLastError() == cudaSuccess ? IGC_OK : IGC_ERR_CUDA;
+  return launch_pdl(shift_widen_rowsum_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                    stream, pp);
 }
 
 }  // namespace prepass
