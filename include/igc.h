@@ -29,10 +29,17 @@
  *    igc_check_device_status() reports it as IGC_ERR_DEVICE_TIMEOUT.
  *  - Alignment: operand base pointers must be 16-byte aligned and operand row
  *    strides (in bytes) multiples of 16 (TMA rules), else IGC_ERR_MISALIGNED.
- *    Outputs may have any alignment; aligned outputs get vector stores.
+ *    Outputs may have any alignment; outputs whose base and row stride are
+ *    16-byte aligned are written by TMA bulk tensor stores, others by direct
+ *    stores.
  *  - Device: an sm_103 GPU (GB300); any other returns IGC_ERR_UNSUPPORTED.
  *  - Calls are stateless and re-entrant; concurrent calls on different streams
  *    are independent (each gemm_s8_zp call needs its own workspace).
+ *  - Launch: kernels use programmatic dependent launch -- a kernel may start
+ *    while the previous kernel in the stream finishes, and waits for it before
+ *    touching memory -- so stream order is kept as with plain launches.  Calls
+ *    may be captured in CUDA graphs; make one call of each operation on the
+ *    device first (per-kernel set-up runs once, outside the capture).
  */
 #ifndef IGC_H
 #define IGC_H
