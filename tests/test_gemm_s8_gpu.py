@@ -167,3 +167,42 @@ def test_whole_tiles_and_split_last_round_bit_exact():
     o32, o8, _ = _oracle(A, Bt, **kw)
     _assert_equal(g32, o32, "C32")
     _assert_equal(g8, o8, "C8")
+
+
+def test_requant_with_non_finite_scales():
+    """Per-column scales holding +inf, -inf, NaN, 0 and the largest finite value:
+    the product is clamped (infinities to the ends), a NaN product gives 0."""
+    rng = np.random.default_rng(12)
+    M, N, K = 128, 256, 64
+    A = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+    Bt = rng.integers(-128, 128, size=(N, K)).astype(np.int8)
+    special = np.array([np.inf, -np.inf, np.nan, 0.0, np.finfo(np.float32).max, 1e-30],
+                       dtype=np.float32)
+    scale_col = np.resize(special, N).astype(np.float32)
+    kw = dict(zA=100, zB=-5, scale_col=scale_col)
+    g32, g8 = _gpu(A, Bt, **kw)
+    o32, o8, _ = _oracle(A, Bt, **kw)
+    _assert_equal(g32, o32, "C32")
+    _assert_equal(g8, o8, "C8")
+
+
+def test_outputs_at_unaligned_addresses_use_direct_stores():
+    """C32 and C8 views that start 4 / 1 bytes past an aligned address: the kernel
+    cannot use TMA stores for them and must write exactly the view."""
+    rng = np.random.default_rng(13)
+    M, N, K = 200, 300, 96
+    A = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+    Bt = rng.integers(0, 256, size=(N, K)).astype(np.uint8)
+    C32big = torch.full((M, N + 4), 9, dtype=torch.int32, device="cuda")
+    C8big = torch.full((M, N + 32), 9, dtype=torch.int8, device="cuda")
+    C32 = C32big[:, 1:1 + N]
+    C8 = C8big[:, 1:1 + N]
+    igc.gemm_s8_zp(dev(A), dev(Bt), zA=7, zB=200, C32=C32, C8=C8,
+                   scale=float(np.float32(2.0 ** -10)))
+    check_device_ok()
+    o32, o8, _ = _oracle(A, Bt, zA=7, zB=200, scale=float(np.float32(2.0 ** -10)))
+    g32, g8 = host(C32big), host(C8big)
+    _assert_equal(g32[:, 1:1 + N], o32, "C32")
+    _assert_equal(g8[:, 1:1 + N], o8, "C8")
+    assert np.all(g32[:, 0] == 9) and np.all(g32[:, 1 + N:] == 9)
+    assert np.all(g8[:, 0] == 9) and np.all(g8[:, 1 + N:] == 9)
