@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
             L.igc_last_device_status.restype = ctypes.c_uint64
             L.igc_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             L.igc_set_wait_limit_ns.restype = ctypes.c_uint64
+            L.igc_set_tile_width.argtypes = [i32]
+            L.igc_set_tile_width.restype = i32
             L.igc_debug_wait_timeout_probe.argtypes = [vp]
             L.igc_debug_wait_timeout_probe.restype = i32
             L.igc_version.argtypes = []
@@ -159,6 +161,10 @@ def igc_check_device_status(stream=None) -> int:
 
 def igc_last_device_status() -> int:
     return int(lib().igc_last_device_status())
+
+
+def igc_set_tile_width(bn: int) -> int:
+    return int(lib().igc_set_tile_width(int(bn)))
 
 
 def igc_set_wait_limit_ns(limit_ns: int) -> int:

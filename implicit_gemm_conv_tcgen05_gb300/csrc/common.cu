@@ -18,6 +18,7 @@ constexpr int kMaxDevices = 64;
 __device__ unsigned long long g_status_word;
 
 std::atomic<unsigned long long> g_wait_limit{2000000000ull};
+std::atomic<int> g_tile_width{0};  // 0: chosen per problem
 std::atomic<unsigned long long> g_last_status{0};
 
 struct DeviceSlot {
@@ -117,6 +118,8 @@ unsigned long long* status_word() {
 
 unsigned long long wait_limit_ns() { return g_wait_limit.load(); }
 
+int tile_width_override() { return g_tile_width.load(); }
+
 int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                     uint32_t box_rows) {
@@ -192,6 +195,11 @@ int igc_check_device_status(igc_stream_t stream) {
 }
 
 uint64_t igc_last_device_status(void) { return igc::g_last_status.load(); }
+
+int igc_set_tile_width(int bn) {
+  if (bn != 0 && bn != 128 && bn != 224 && bn != 256) return -1;
+  return igc::g_tile_width.exchange(bn);
+}
 
 uint64_t igc_set_wait_limit_ns(uint64_t limit_ns) {
   if (limit_ns < 1000) limit_ns = 1000;

@@ -109,6 +109,8 @@ struct TileCfg {
   static constexpr size_t kSmemBytes =
       1024 + kStages * kStageBytes + kStagingBytes + kBarrierBytes;
   static constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256 : 512;  // power of two >= 2*BN
+  // column of accumulator 1 (a multiple of 32, so every tcgen05.ld starts aligned)
+  static constexpr uint32_t kAccStride = kTmemCols / 2;
   static constexpr int kEpiCols = BN / 2;  // columns per epilogue warp
 };
 
@@ -221,40 +223,49 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits) {
     return pack_half2(lo_bits, hi_bits);
 }
 
+// Direct stores of columns c0 .. c1-1 of row m (a row per thread; c0 and c1
+// multiples of 8, constants after inlining where the tile width allows).
+// vec: 16-byte stores allowed for groups that lie inside the matrix.
 template <int NC, bool kBf16>
-__device__ __forceinline__ void store_row_16bit(void* out, long long ldo, int M, int N, int m,
-                                                int n0, bool full, const uint32_t (&v)[NC]) {
+__device__ __forceinline__ void store_cols_16bit(void* out, long long ldo, int N, int m, int n0,
+                                                 bool vec, int c0, int c1,
+                                                 const uint32_t (&v)[NC]) {
+  static_assert(NC % 8 == 0, "16-byte groups");
   uint16_t* row = reinterpret_cast<uint16_t*>(out) + static_cast<size_t>(m) * ldo + n0;
-  if (full) {
 #pragma unroll
-    for (int j = 0; j < NC / 8; ++j) {
+  for (int j = 0; j < NC / 8; ++j) {
+    if (8 * j < c0 || 8 * j >= c1) continue;
+    if (vec && n0 + 8 * j + 8 <= N) {
       uint4 q;
       q.x = pack2<kBf16>(v[8 * j + 0], v[8 * j + 1]);
       q.y = pack2<kBf16>(v[8 * j + 2], v[8 * j + 3]);
       q.z = pack2<kBf16>(v[8 * j + 4], v[8 * j + 5]);
       q.w = pack2<kBf16>(v[8 * j + 6], v[8 * j + 7]);
       reinterpret_cast<uint4*>(row)[j] = q;
-    }
-  } else {
+    } else {
 #pragma unroll
-    for (int i = 0; i < NC; ++i)
-      if (n0 + i < N) row[i] = static_cast<uint16_t>(pack2<kBf16>(v[i], 0u) & 0xFFFFu);
+      for (int i = 8 * j; i < 8 * j + 8; ++i)
+        if (n0 + i < N) row[i] = static_cast<uint16_t>(pack2<kBf16>(v[i], 0u) & 0xFFFFu);
+    }
   }
 }
 
 template <int NC>
-__device__ __forceinline__ void store_row_f32(float* out, long long ldo, int N, int m, int n0,
-                                              bool full, const uint32_t (&v)[NC]) {
+__device__ __forceinline__ void store_cols_f32(float* out, long long ldo, int N, int m, int n0,
+                                               bool vec, int c0, int c1, const uint32_t (&v)[NC]) {
+  static_assert(NC % 4 == 0, "16-byte groups");
   float* row = out + static_cast<size_t>(m) * ldo + n0;
-  if (full) {
 #pragma unroll
-    for (int j = 0; j < NC / 4; ++j)
+  for (int j = 0; j < NC / 4; ++j) {
+    if (4 * j < c0 || 4 * j >= c1) continue;
+    if (vec && n0 + 4 * j + 4 <= N) {
       reinterpret_cast<uint4*>(row)[j] =
           make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-  } else {
+    } else {
 #pragma unroll
-    for (int i = 0; i < NC; ++i)
-      if (n0 + i < N) row[i] = __uint_as_float(v[i]);
+      for (int i = 4 * j; i < 4 * j + 4; ++i)
+        if (n0 + i < N) row[i] = __uint_as_float(v[i]);
+    }
   }
 }
 
@@ -284,12 +295,14 @@ struct Stager {
   }
 };
 
-// 32-bit values (fp32 / int32 bit patterns), boxes of 32 columns.
+// 32-bit values (fp32 / int32 bit patterns), boxes of 32 columns: the boxes that
+// lie wholly inside the first nvalid columns.
 template <int NC>
 __device__ __forceinline__ void stage_store_u32(const Stager& st, const CUtensorMap* map, int n0,
-                                                const uint32_t (&v)[NC]) {
+                                                const uint32_t (&v)[NC], int nvalid = NC) {
 #pragma unroll
   for (int b = 0; b < NC / 32; ++b) {
+    if (32 * b + 32 > nvalid) continue;
     st.begin();
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -299,12 +312,14 @@ __device__ __forceinline__ void stage_store_u32(const Stager& st, const CUtensor
   }
 }
 
-// fp32 values rounded to fp16 / bf16, boxes of 64 columns.
+// fp32 values rounded to fp16 / bf16, boxes of 64 columns: the boxes that lie
+// wholly inside the first nvalid columns.
 template <int NC, bool kBf16>
 __device__ __forceinline__ void stage_store_16bit(const Stager& st, const CUtensorMap* map, int n0,
-                                                  const uint32_t (&v)[NC]) {
+                                                  const uint32_t (&v)[NC], int nvalid = NC) {
 #pragma unroll
   for (int b = 0; b < NC / 64; ++b) {
+    if (64 * b + 64 > nvalid) continue;
     st.begin();
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -316,36 +331,40 @@ __device__ __forceinline__ void stage_store_16bit(const Stager& st, const CUtens
   }
 }
 
-// Row m of the tile, columns n0 .. n0+NC-1, values v (fp32 bit patterns).  Every
-// lane of the warp must call it (the TMA path is warp-collective); rows past M
-// are clipped by the store.
+// Row m of the tile, columns n0 .. n0+nvalid-1 (nvalid <= NC; the warp holds NC
+// columns), values v (fp32 bit patterns).  Every lane of the warp must call it
+// (the TMA path is warp-collective); rows past M are clipped by the store.
+// Columns past the last whole TMA box inside nvalid are stored directly.
 template <int NC>
 __device__ __forceinline__ void store_row_float(const KParams& p, const CUtensorMap& tmO0,
                                                 const CUtensorMap& tmO1, const Stager& st, int m,
-                                                int n0, const uint32_t (&v)[NC]) {
-  const bool full = p.vec_ok && (n0 + NC <= p.N);
+                                                int n0, const uint32_t (&v)[NC],
+                                                int nvalid = NC) {
+  const int boxed16 = nvalid / 64 * 64;  // columns stored by whole 16-bit boxes
+  const int boxed32 = nvalid / 32 * 32;  // columns stored by whole 32-bit boxes
+  const bool in_row = m < p.M;
   if (p.out != nullptr) {
-    if (p.tma_out & 1) {
-      if (p.out_type == kOutF16)
-        stage_store_16bit<NC, false>(st, &tmO0, n0, v);
-      else if (p.out_type == kOutBF16)
-        stage_store_16bit<NC, true>(st, &tmO0, n0, v);
-      else
-        stage_store_u32<NC>(st, &tmO0, n0, v);
-    } else if (m < p.M) {
-      if (p.out_type == kOutF16)
-        store_row_16bit<NC, false>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
-      else if (p.out_type == kOutBF16)
-        store_row_16bit<NC, true>(p.out, p.ldo, p.M, p.N, m, n0, full, v);
-      else
-        store_row_f32<NC>(reinterpret_cast<float*>(p.out), p.ldo, p.N, m, n0, full, v);
+    const bool tma = p.tma_out & 1;
+    if (p.out_type == kOutF16) {
+      if (tma) stage_store_16bit<NC, false>(st, &tmO0, n0, v, nvalid);
+      if (in_row)
+        store_cols_16bit<NC, false>(p.out, p.ldo, p.N, m, n0, p.vec_ok, tma ? boxed16 : 0, nvalid, v);
+    } else if (p.out_type == kOutBF16) {
+      if (tma) stage_store_16bit<NC, true>(st, &tmO0, n0, v, nvalid);
+      if (in_row)
+        store_cols_16bit<NC, true>(p.out, p.ldo, p.N, m, n0, p.vec_ok, tma ? boxed16 : 0, nvalid, v);
+    } else {
+      if (tma) stage_store_u32<NC>(st, &tmO0, n0, v, nvalid);
+      if (in_row)
+        store_cols_f32<NC>(reinterpret_cast<float*>(p.out), p.ldo, p.N, m, n0, p.vec_ok,
+                           tma ? boxed32 : 0, nvalid, v);
     }
   }
   if (p.out_f32 != nullptr) {
-    if (p.tma_out & 2)
-      stage_store_u32<NC>(st, &tmO1, n0, v);
-    else if (m < p.M)
-      store_row_f32<NC>(p.out_f32, p.ldo32, p.N, m, n0, full, v);
+    const bool tma = p.tma_out & 2;
+    if (tma) stage_store_u32<NC>(st, &tmO1, n0, v, nvalid);
+    if (in_row)
+      store_cols_f32<NC>(p.out_f32, p.ldo32, p.N, m, n0, p.vec_ok, tma ? boxed32 : 0, nvalid, v);
   }
 }
 
@@ -621,6 +640,27 @@ __device__ __forceinline__ void tmem_drain(uint32_t taddr, uint32_t (&sum)[NC], 
   }
 }
 
+// One warp's float epilogue for a unit: NCX accumulator columns from TMEM
+// address taddr, the accumulator released (arrival on the leader's `tempty`)
+// as soon as they are in registers, then row m's outputs at columns
+// n0 .. n0+nvalid-1.
+// Inactive warps (the idle half of a half unit) only take part in the release.
+template <int NCX>
+__device__ __forceinline__ void epi_float_cols(const KParams& p, const CUtensorMap& tmO0,
+                                               const CUtensorMap& tmO1, const Stager& st,
+                                               uint32_t taddr, int m, int n0, int nvalid,
+                                               bool active, uint32_t release_bar, int lane) {
+  uint32_t v[NCX];
+  if (active) {
+    tmem_load_cols<NCX>(taddr, v);
+    tmem_ld_wait();
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_remote(release_bar);
+  if (active) store_row_float<NCX>(p, tmO0, tmO1, st, m, n0, v, nvalid);
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -815,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             const uint64_t a_st = adesc0 + ((static_cast<uint32_t>(stage) * kStageABytes) >> 4);
             const uint64_t b_st = bdesc0 + ((static_cast<uint32_t>(stage) * Cfg::kStageBBytes) >> 4);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * Cfg::kAccStride;
 #pragma unroll
             for (int j = 0; j < kAtoms; ++j) {
 #pragma unroll
@@ -861,6 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // tcgen05.ld: warp w may access lanes 32*(w%4) .. +31
     const int half = ew >> 2;   // which column half of the tile
     const int row_in_cta = quad * 32 + lane;
+    // TMEM address of this warp's lanes and column half (integer modes)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(half * NC);
     const int n_chunks =
@@ -889,17 +930,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                         p.status, kSiteEpiFull)))
           goto epi_done;
         tc_fence_after();
-        uint32_t v[NC];
-        if (active) {
-          tmem_load_cols<NC>(lane_base + static_cast<uint32_t>(acc * BN), v);
-          tmem_ld_wait();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
+        const uint32_t rel = tempty_lead + static_cast<uint32_t>(acc) * 8u;
+        const uint32_t acc_cols = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                  static_cast<uint32_t>(acc) * Cfg::kAccStride;
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
-        if (active) store_row_float<NC>(p, tmO0, tmO1, st, m, n0, v);
+        if constexpr (BN == 224) {
+          // every warp loads 128 columns from a 32-aligned column (0 or 128) and
+          // stores the ones its unit owns: 128 + 96 for a whole tile, 112 (from
+          // column 0, half-0 warps) for a half unit
+          const int col = w.half ? 0 : half * 128;
+          const int nvalid = w.half ? BN / 2 : (half == 0 ? 128 : BN - 128);
+          epi_float_cols<128>(p, tmO0, tmO1, st, acc_cols + static_cast<uint32_t>(col), m,
+                              w.half ? n0 : w.nb * BN + col, nvalid, active, rel, lane);
+        } else {
+          epi_float_cols<NC>(p, tmO0, tmO1, st, acc_cols + static_cast<uint32_t>(half * NC), m,
+                             n0, NC, active, rel, lane);
+        }
       } else {
         uint32_t sum[NC];
 #pragma unroll
@@ -910,7 +957,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             goto epi_done;
           tc_fence_after();
           if (active)
-            tmem_drain<NC>(lane_base + static_cast<uint32_t>(acc * BN), sum, c == 0 && first_exact);
+            tmem_drain<NC>(lane_base + static_cast<uint32_t>(acc) * Cfg::kAccStride, sum,
+                           c == 0 && first_exact);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);

@@ -162,10 +162,15 @@ inline int pick_bn(long long M, long long N, int clusters, const int* cands, con
 }
 
 // Tile widths each operation is built for, with their relative mainloop
-// efficiency (wider tiles move fewer operand bytes per flop).
-constexpr int kBnCands[] = {256, 128};
-constexpr double kBnEff[] = {1.0, 0.87};  // measured: fp16 8192^3 at BN 128 runs 0.87x BN 256
-constexpr int kNumBn = sizeof(kBnCands) / sizeof(kBnCands[0]);
+// efficiency (wider tiles move fewer operand bytes per flop).  224 lets skinny
+// problems fill the CTA pairs (e.g. 8192 columns = 37 tiles of 224 instead of
+// 32 of 256); the integer modes drain in 64-column steps and use 256 and 128.
+constexpr int kBnCands[] = {256, 224, 128};
+// measured on fp16 M x 8192 x 8192 with many rounds: BN 224 runs 0.987x and
+// BN 128 0.87-0.92x the rate of BN 256
+constexpr double kBnEff[] = {1.0, 0.97, 0.87};
+constexpr int kBnCandsInt[] = {256, 128};
+constexpr double kBnEffInt[] = {1.0, 0.87};
 
 // Picks the tile width for this problem, encodes B's tensor map with a box of
 // BN/2 rows (each CTA of the pair loads half of the B tile) and launches.
@@ -179,11 +184,16 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
   int clusters = 0;
   int rc = kernel_setup<kMode, kBnCands[0]>(dev, &clusters);
   if (rc != IGC_OK) return rc;
-  const int bn = pick_bn(p.M, p.N, clusters, kBnCands, kBnEff, kNumBn);
+  int bn = mode_is_int(kMode) ? pick_bn(p.M, p.N, clusters, kBnCandsInt, kBnEffInt, 2)
+                              : pick_bn(p.M, p.N, clusters, kBnCands, kBnEff, 3);
+  const int forced = tile_width_override();
+  if (forced == 256 || forced == 128 || (forced == 224 && !mode_is_int(kMode))) bn = forced;
   CUtensorMap tmB;
   rc = encode_tiled_2d(&tmB, kBType, b_base, b_inner, b_rows,
                        b_row_bytes, BK, static_cast<uint32_t>(bn / 2));
   if (rc != IGC_OK) return rc;
+  if constexpr (!mode_is_int(kMode))
+    if (bn == 224) return launch_tc_gemm<kMode, 224>(dev, tmA, tmB, om, p, stream);
   switch (bn) {
     case 256: return launch_tc_gemm<kMode, 256>(dev, tmA, tmB, om, p, stream);
     case 128: return launch_tc_gemm<kMode, 128>(dev, tmA, tmB, om, p, stream);

@@ -341,6 +341,17 @@ uint64_t igc_last_device_status(void);
 uint64_t igc_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
+ * Tuning and test hook: the output tile width (columns of B per CTA pair) of
+ * every GEMM / convolution launched after this call.  0 (the default) picks it
+ * per problem; 128, 224 or 256 force it where the operation is built for it
+ * (the integer paths have 128 and 256; a width an operation lacks is ignored
+ * for it).  Results do not depend on the width beyond fp32 rounding order
+ * (integer results are identical).  Returns the previous setting, or -1 (and
+ * changes nothing) for any other value.  Process-wide.
+ */
+int igc_set_tile_width(int bn);
+
+/*
  * Diagnostic: launches one CTA that waits on an mbarrier nothing ever
  * completes, with the current wait limit, and returns.  The wait gives up
  * after the limit and records IGC_ERR_DEVICE_TIMEOUT for

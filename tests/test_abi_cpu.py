@@ -17,7 +17,8 @@ def test_library_loads_and_exports_every_declared_symbol():
                 "gemm_s8_zp_run", "gemm_s8_zp_dequant", "gemm_s8_zp_noalloc",
                 "conv2d_nhwc_s8_zp", "conv2d_nhwc_s8_zp_workspace_size", "conv2d_nhwc_f16_implicit",
                 "igc_status_string", "igc_check_device_status", "igc_last_device_status",
-                "igc_set_wait_limit_ns", "igc_debug_wait_timeout_probe", "igc_version"}
+                "igc_set_wait_limit_ns", "igc_set_tile_width", "igc_debug_wait_timeout_probe",
+                "igc_version"}
     assert expected <= set(names)
     for n in names:
         assert hasattr(L, n), n
@@ -97,3 +98,10 @@ def test_header_declares_c_linkage_and_statuses():
                        ("IGC_ERR_WORKSPACE", 6), ("IGC_F32", 0), ("IGC_F16", 1), ("IGC_BF16", 2)]:
         assert re.search(rf"#define {name} {code}\b", text)
         assert getattr(igc, name) == code
+
+
+def test_tile_width_setter_roundtrip():
+    assert igc.igc_set_tile_width(224) == 0
+    assert igc.igc_set_tile_width(96) == -1          # not a built width: unchanged
+    assert igc.igc_set_tile_width(128) == 224
+    assert igc.igc_set_tile_width(0) == 128
