@@ -59,7 +59,6 @@ extern "C" int conv2d_nhwc_f16_implicit(int N, int H, int W, int C, int K, int R
   p.conv_cblocks = (C + KS - 1) / KS;
   p.num_kb = R * S * p.conv_cblocks;
   p.chunk_kb = p.num_kb;
-  p.first_kb = p.num_kb;
   p.conv_P = static_cast<int>(P);
   p.conv_Q = static_cast<int>(Q);
   p.conv_S = S;

@@ -299,7 +299,6 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
   p.conv_cblocks = (C + KS - 1) / KS;
   p.num_kb = R * S * p.conv_cblocks;
   p.chunk_kb = kIntChunkKb;
-  p.first_kb = kIntFirstChunkKb;
   p.conv_P = static_cast<int>(c.P);
   p.conv_Q = static_cast<int>(c.Q);
   p.conv_S = S;

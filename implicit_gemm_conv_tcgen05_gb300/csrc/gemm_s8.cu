@@ -8,10 +8,11 @@
 //     B' = B_q - oB with oX = 128 for uint8, 0 for int8, so every value lies in
 //     [-128, 127] and is exact in fp16; written as fp16 into the workspace
 //     together with the sums rA'[i] = sum_k A'[i,k] and cB'[j] = sum_k B'[j,k].
-//  2. tcgen05 kind::f16 GEMM over A', B' in chunks of 256 k: each chunk's
-//     partial sums are integers of magnitude <= 256 * 128 * 128 = 2^22, so the
-//     fp32 accumulator holds them exactly; the epilogue drains every chunk into
-//     an int32 running sum S'[i,j] = sum_k A'[i,k] B'[j,k].
+//  2. tcgen05 kind::f16 GEMM over A', B' in chunks of 1024 k: each chunk's
+//     partial sums are integers of magnitude <= 1024 * 128 * 128 = 2^24, so the
+//     fp32 accumulator holds them exactly; the epilogue drains every chunk
+//     (exact float-to-int conversion) into an int32 running sum
+//     S'[i,j] = sum_k A'[i,k] B'[j,k].
 //  3. fused epilogue, in int32 two's complement (mod 2^32):
 //        C32 = S' - zB'_j rA'_i - zA'_i cB'_j + K zA'_i zB'_j,
 //     with zA'_i = zA_i - oA and zB'_j = zB_j - oB -- the zero-point expansion of
@@ -154,7 +155,6 @@ int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, in
   p.K = static_cast<int>(K);
   p.num_kb = static_cast<int>((Kp + KS - 1) / KS);
   p.chunk_kb = kIntChunkKb;
-  p.first_kb = kIntFirstChunkKb;
   p.c32 = C32;
   p.ldc32 = ldc32;
   p.c8 = C8;

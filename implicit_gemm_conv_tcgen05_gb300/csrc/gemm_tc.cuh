@@ -44,12 +44,11 @@
 // CTA pairs, that round's tiles run as two BN/2-wide column halves.
 //
 // The integer modes accumulate in chunks that fp32 holds exactly: products of
-// the shifted operands are integers of magnitude <= 2^14, so a chunk of 256 k
-// stays within 2^22 and one of 1024 k within 2^24.  Each unit's first chunk
-// (up to 1024 k) is drained into the int32 running sums by an exact
-// float-to-int conversion, every later 256-k chunk by the round-to-integer
-// trick x + 1.5*2^23.  The long first chunk lets the main loop run ahead while
-// the epilogue finishes the previous unit.
+// the shifted operands are integers of magnitude <= 2^14, so every partial sum
+// of a 1024-k chunk is an integer of magnitude <= 2^24.  Each chunk is drained
+// into the int32 running sums by a float-to-int conversion toward zero, exact
+// for integral values; a chunk's MMAs (about 5 us) let the main loop run ahead
+// while the epilogue finishes the previous unit.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -92,8 +91,7 @@ constexpr uint32_t kBarrierBytes = 512;
 constexpr uint32_t kStagingWarpBytes = 32 * 128;
 constexpr uint32_t kStagingBytes = kEpiWarps * kStagingWarpBytes;
 constexpr size_t kSmemBudget = 227 * 1024;
-constexpr int kIntChunkKb = 256 / KS;         // stages per chunk drained by x + 1.5*2^23
-constexpr int kIntFirstChunkKb = 1024 / KS;   // stages of a unit's first chunk (exact drain)
+constexpr int kIntChunkKb = 1024 / KS;  // stages per exact fp32 accumulation chunk (1024 k)
 
 template <int BN>
 struct TileCfg {
@@ -132,8 +130,7 @@ struct KParams {
   // persistent schedule: tiles before tail_start are whole work units; every
   // tile from tail_start on is split into two column halves (num_units in all)
   int tail_start, num_units;
-  int chunk_kb;  // k-blocks per accumulation chunk ...
-  int first_kb;  // ... except the first chunk of each unit, which has first_kb
+  int chunk_kb;  // k-blocks per accumulation chunk (an accumulator hand-off after each)
   int conv_P, conv_Q, conv_cblocks, conv_S, conv_C;
   int pad_h, pad_w, stride_h, stride_w;
   void* out;
@@ -422,20 +419,18 @@ __device__ __forceinline__ uint32_t col_val(const uint32_t (&v)[NB], int c) {
 //   C32 = S' - zB'_j (rA'_i - K zA'_i) - zA'_i cB'_j          (int32, mod 2^32)
 // which equals S' - zB'_j rA'_i - zA'_i cB'_j + K zA'_i zB'_j.
 struct IntRow {
-  uint32_t bias;       // n_magic * 0x4B400000 carried by the running sums
   uint32_t zAp;        // zA'_i
   uint32_t u;          // rA'_i - K zA'_i
-  uint32_t t_uniform;  // zB' u + bias when zB is per tensor
+  uint32_t t_uniform;  // zB' u when zB is per tensor
   float sA;            // dequantisation row scale
 };
 
-__device__ __forceinline__ IntRow int_row(const KParams& p, int m, int n_magic) {
+__device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
   const int mm = m < p.M ? m : p.M - 1;  // rows past M are computed (and clipped) like row M-1
   IntRow r;
-  r.bias = static_cast<uint32_t>(n_magic) * 0x4B400000u;
   r.zAp = static_cast<uint32_t>((p.zA_row ? __ldg(p.zA_row + mm) : p.zA) - p.oA);
   r.u = static_cast<uint32_t>(__ldg(p.rsumA + mm)) - static_cast<uint32_t>(p.K) * r.zAp;
-  r.t_uniform = static_cast<uint32_t>(p.zB - p.oB) * r.u + r.bias;
+  r.t_uniform = static_cast<uint32_t>(p.zB - p.oB) * r.u;
   r.sA = p.dq_row ? __ldg(p.dq_row + mm) : 1.0f;
   return r;
 }
@@ -447,7 +442,7 @@ __device__ __forceinline__ void int_group(const KParams& p, const IntRow& r, con
   if (p.zB_col) {
 #pragma unroll
     for (int i = 0; i < kG; ++i)
-      c[i] = static_cast<int32_t>(sum[j * kG + i] - r.bias -
+      c[i] = static_cast<int32_t>(sum[j * kG + i] -
                                   (col_val(V.zB, j * kG + i) - static_cast<uint32_t>(p.oB)) * r.u -
                                   r.zAp * col_val(V.cB, j * kG + i));
   } else {
@@ -488,7 +483,7 @@ __device__ __forceinline__ void float_group(const KParams& p, const IntRow& r,
   }
 }
 
-// sum[] holds, per column, n_magic * 0x4B400000 + sum_k A'B' (mod 2^32).  Writes
+// sum[] holds, per column, sum_k A'B' (mod 2^32).  Writes
 // the requested integer-mode outputs of row m, columns n0 .. n0+NC-1.  Every lane
 // of the warp must call it and run every group: the column values are broadcast
 // by shuffles and the TMA paths are warp-collective; only the direct stores are
@@ -497,8 +492,8 @@ template <int NC>
 __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMap& tmO0,
                                               const CUtensorMap& tmO1, const CUtensorMap& tmO2,
                                               const Stager& st, int m, int n0,
-                                              const uint32_t (&sum)[NC], int n_magic) {
-  const IntRow r = int_row(p, m, n_magic);
+                                              const uint32_t (&sum)[NC]) {
+  const IntRow r = int_row(p, m);
   ColVecs<NC> V;
   load_col_vecs<NC>(p, n0, st.lane, V);
   const bool in_row = m < p.M;
@@ -609,14 +604,11 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&v)[NC]
   }
 }
 
-// Drains NC fp32 TMEM columns that hold exact integers into the running sums,
-// two 32-column loads per wait.  exact: the chunk may reach |x| <= 2^24 (up to
-// 1024 products of magnitude <= 2^14, every partial sum an integer fp32 holds
-// exactly); the sums are set to x converted toward zero, exact for integral
-// values.  Otherwise |x| <= 2^22 and the bits of x + 1.5*2^23, i.e. 0x4B400000 + x,
-// are added to the sums.
+// Drains NC fp32 TMEM columns holding the exact integer sums of one chunk into
+// the int32 running sums (set by the first chunk, added after it), two
+// 32-column loads per wait.  Conversion toward zero is exact for integral values.
 template <int NC>
-__device__ __forceinline__ void tmem_drain(uint32_t taddr, uint32_t (&sum)[NC], bool exact) {
+__device__ __forceinline__ void tmem_drain(uint32_t taddr, uint32_t (&sum)[NC], bool first) {
   static_assert(NC % 64 == 0, "drain in steps of 64 columns");
 #pragma unroll
   for (int j = 0; j < NC / 64; ++j) {
@@ -624,18 +616,12 @@ __device__ __forceinline__ void tmem_drain(uint32_t taddr, uint32_t (&sum)[NC], 
     tmem_ld_32x32b_x32(taddr + j * 64, r0);
     tmem_ld_32x32b_x32(taddr + j * 64 + 32, r1);
     tmem_ld_wait();
-    if (exact) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sum[j * 64 + i] = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r0[i])));
-        sum[j * 64 + 32 + i] = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r1[i])));
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sum[j * 64 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r0[i]), 12582912.0f));
-        sum[j * 64 + 32 + i] += __float_as_uint(__fadd_rn(__uint_as_float(r1[i]), 12582912.0f));
-      }
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t a0 = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r0[i])));
+      const uint32_t a1 = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r1[i])));
+      sum[j * 64 + i] = first ? a0 : sum[j * 64 + i] + a0;
+      sum[j * 64 + 32 + i] = first ? a1 : sum[j * 64 + 32 + i] + a1;
     }
   }
 }
@@ -839,7 +825,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = cluster; u < p.num_units; u += num_clusters) {
         const uint32_t idesc = u >= p.tail_start ? idesc_half : idesc_full;
         int kin = 0;
-        int clen = p.first_kb;  // length of the current chunk
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (kin == 0) {
             if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, lim, abort_flag,
@@ -851,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   kSiteMmaFull)))
             goto mma_done_label;
           tc_fence_after();
-          const bool chunk_end = (kin == clen - 1) || (kb == p.num_kb - 1);
+          const bool chunk_end = (kin == p.chunk_kb - 1) || (kb == p.num_kb - 1);
           if (lane == 0) {
             const uint64_t a_st = adesc0 + ((static_cast<uint32_t>(stage) * kStageABytes) >> 4);
             const uint64_t b_st = bdesc0 + ((static_cast<uint32_t>(stage) * Cfg::kStageBBytes) >> 4);
@@ -873,10 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
           }
-          if (++kin == clen) {
-            kin = 0;
-            clen = p.chunk_kb;
-          }
+          if (++kin == p.chunk_kb) kin = 0;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -904,12 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMEM address of this warp's lanes and column half (integer modes)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(half * NC);
-    const int n_chunks =
-        1 + (p.num_kb > p.first_kb ? (p.num_kb - p.first_kb + p.chunk_kb - 1) / p.chunk_kb : 0);
-    // a first chunk longer than 256 k is drained by an exact float-to-int
-    // conversion; every other chunk carries 0x4B400000 into the running sums
-    const bool first_exact = p.first_kb > kIntChunkKb;
-    const int n_magic = n_chunks - (first_exact ? 1 : 0);
+    const int n_chunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
     Stager st;
     st.buf = staging + ew * kStagingWarpBytes;
     st.lane = lane;
@@ -957,15 +934,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             goto epi_done;
           tc_fence_after();
           if (active)
-            tmem_drain<NC>(lane_base + static_cast<uint32_t>(acc) * Cfg::kAccStride, sum,
-                           c == 0 && first_exact);
+            tmem_drain<NC>(lane_base + static_cast<uint32_t>(acc) * Cfg::kAccStride, sum, c == 0);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
-        if (active) store_row_int<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum, n_magic);
+        if (active) store_row_int<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum);
       }
     }
   epi_done:

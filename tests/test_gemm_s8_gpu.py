@@ -70,10 +70,11 @@ def test_config5_8192_cubed_sampled_rows_bit_exact():
 @pytest.mark.parametrize("a_val,b_val,a_signed,b_signed", [
     (255, 255, 0, 0), (0, 255, 0, 0), (255, 0, 0, 0), (-128, -128, 1, 1), (127, -128, 1, 1),
     (255, -128, 0, 1), (0, 127, 0, 1)])
-@pytest.mark.parametrize("K", [256, 512, 4096 + 256])
+@pytest.mark.parametrize("K", [256, 512, 1024, 4096 + 256])
 def test_extreme_magnitudes_exact(a_val, b_val, a_signed, b_signed, K):
     """Constant operands at the ends of their ranges: every fp32 chunk sum sits
-    at its largest magnitude (2^22), testing the exactness of the chunking."""
+    at its largest magnitude (2^24 for a full 1024-k chunk of (-128)(-128)
+    products), testing the exactness of the chunking."""
     M, N = 128, 256
     A = np.full((M, K), a_val, np.int8 if a_signed else np.uint8)
     Bt = np.full((N, K), b_val, np.int8 if b_signed else np.uint8)
