@@ -366,13 +366,13 @@ __device__ __forceinline__ void store_row_float(const KParams& p, const CUtensor
 }
 
 // Requantisation of one int32 result: fp32(c) rounded to nearest even, one fp32
-// multiply, clamp to [-128, 127] (a NaN product gives 0), then round half to
-// even by adding 1.5*2^23 (exact for |f| <= 2^22: the sum's ulp is 1, so the
-// fp32 add rounds f to the nearest integer, ties to even).  Returns the byte.
+// multiply, then one conversion to int8 that rounds to nearest even and
+// saturates to [-128, 127] (a NaN product converts to 0).  Returns the byte.
 __device__ __forceinline__ uint32_t requant_byte(int32_t c, float s) {
-  float f = __fmul_rn(__int2float_rn(c), s);
-  f = (f == f) ? fminf(fmaxf(f, -128.0f), 127.0f) : 0.0f;
-  return static_cast<uint32_t>(__float_as_int(__fadd_rn(f, 12582912.0f)) - 0x4B400000) & 0xFFu;
+  const float f = __fmul_rn(__int2float_rn(c), s);
+  int32_t q;
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(q) : "f"(f));
+  return static_cast<uint32_t>(q) & 0xFFu;
 }
 
 constexpr int kG = 16;  // columns per step of the integer epilogue
@@ -616,12 +616,18 @@ __device__ __forceinline__ void tmem_drain(uint32_t taddr, uint32_t (&sum)[NC], 
     tmem_ld_32x32b_x32(taddr + j * 64, r0);
     tmem_ld_32x32b_x32(taddr + j * 64 + 32, r1);
     tmem_ld_wait();
+    if (first) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t a0 = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r0[i])));
-      const uint32_t a1 = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r1[i])));
-      sum[j * 64 + i] = first ? a0 : sum[j * 64 + i] + a0;
-      sum[j * 64 + 32 + i] = first ? a1 : sum[j * 64 + 32 + i] + a1;
+      for (int i = 0; i < 32; ++i) {
+        sum[j * 64 + i] = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r0[i])));
+        sum[j * 64 + 32 + i] = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r1[i])));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        sum[j * 64 + i] += static_cast<uint32_t>(__float2int_rz(__uint_as_float(r0[i])));
+        sum[j * 64 + 32 + i] += static_cast<uint32_t>(__float2int_rz(__uint_as_float(r1[i])));
+      }
     }
   }
 }
