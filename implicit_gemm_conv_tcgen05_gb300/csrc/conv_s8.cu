@@ -30,6 +30,7 @@ namespace igc {
 namespace conv_s8 {
 
 constexpr size_t kWsAlign = 256;
+constexpr int kEpilogueWindowMax = 25;  // filter windows up to 5 x 5 are summed in the epilogue
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct ConvShape {
@@ -129,13 +130,21 @@ static __global__ void __launch_bounds__(256) pad_shift_pixels_kernel(
 // two <= 32, so the G threads of a pixel are an aligned group of lanes of one
 // warp: x' = x_q - oX inside the image (exact fp16 by the pre-pass's byte
 // widening), zX - oX in the border; lane 0 of the group writes the pixel's
-// channel sum.  Threads past the end still take part in the shuffles.
+// channel sum.  Threads past the end still take part in the shuffles.  The
+// first w_blocks blocks widen the weights instead (one row of wop per warp), so
+// that both operands' pre-passes are one launch.
 static __global__ void __launch_bounds__(256) pad_shift_chunks_kernel(
     const uint8_t* __restrict__ x, uint32_t flip, int border, int N, int H, int W, int C, int ph,
-    int pw, int Hp, int Wp, int log2g, __half* __restrict__ xp, int32_t* __restrict__ px) {
+    int pw, int Hp, int Wp, int log2g, __half* __restrict__ xp, int32_t* __restrict__ px,
+    unsigned w_blocks, const PrepassOperand wop, int wK, int wKp) {
   grid_dependency_wait();
   grid_dependents_launch();
-  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (blockIdx.x < w_blocks) {
+    const int row = static_cast<int>(blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32);
+    if (row < wop.rows) widen_row(wop, row, wK, wKp, static_cast<int>(threadIdx.x % 32));
+    return;
+  }
+  const long long t = static_cast<long long>(blockIdx.x - w_blocks) * blockDim.x + threadIdx.x;
   const long long npix = static_cast<long long>(N) * Hp * Wp;
   const bool valid = t < (npix << log2g);
   const long long pixel = t >> log2g;
@@ -252,7 +261,10 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
   const int oX = x_signed ? 0 : 128;
   const int oW = w_signed ? 0 : 128;
 
-  // 1. padded, shifted input and its pixel sums
+  // 1. padded, shifted input and its pixel sums (with the chunked pass, the
+  //    weights of step 2 go through the same launch)
+  const PrepassOperand wop = prepass_operand(w, c.Kg, K, c.Kg, c.Kgp, w_signed ? 1 : 0, wp, cw);
+  bool weights_done = false;
   {
     const long long npix = c.N * c.Hp * c.Wp;
     const int vec = (C % 16 == 0) && aligned16(x);
@@ -261,10 +273,16 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
       int log2g = 0;
       while ((1 << log2g) < groups) ++log2g;
       const long long threads = npix << log2g;
-      rc = launch_pdl(pad_shift_chunks_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)),
+      const long long pix_blocks = (threads + 255) / 256;
+      const long long w_blocks = (static_cast<long long>(K) + 7) / 8;  // 8 weight rows per block
+      if (pix_blocks + w_blocks >= (1LL << 31)) return IGC_ERR_UNSUPPORTED;
+      rc = launch_pdl(pad_shift_chunks_kernel, dim3(static_cast<unsigned>(pix_blocks + w_blocks)),
                       dim3(256), 0, stream, static_cast<const uint8_t*>(x),
                       x_signed ? 0x80808080u : 0u, zX - oX, N, H, W, C, pad_h, pad_w,
-                      static_cast<int>(c.Hp), static_cast<int>(c.Wp), log2g, xp, px);
+                      static_cast<int>(c.Hp), static_cast<int>(c.Wp), log2g, xp, px,
+                      static_cast<unsigned>(w_blocks), wop, static_cast<int>(c.Kg),
+                      static_cast<int>(c.Kgp));
+      weights_done = true;
     } else {
       rc = launch_pdl(pad_shift_pixels_kernel, dim3(static_cast<unsigned>((npix + 7) / 8)),
                       dim3(256), 0, stream, static_cast<const uint8_t*>(x), x_signed ? 1 : 0, oX,
@@ -274,17 +292,20 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
     if (rc != IGC_OK) return rc;
   }
   // 2. weights: K rows of R*S*C values
-  {
-    PrepassOperand op = prepass_operand(w, c.Kg, K, c.Kg, c.Kgp, w_signed ? 1 : 0, wp, cw);
-    rc = launch_prepass(&op, 1, c.Kg, c.Kgp, stream);
+  if (!weights_done) {
+    rc = launch_prepass(&wop, 1, c.Kg, c.Kgp, stream);
     if (rc != IGC_OK) return rc;
   }
-  // 3. window sums of the im2col rows
-  rc = launch_pdl(window_sums_kernel, dim3(static_cast<unsigned>((c.M + 255) / 256)), dim3(256),
-                  0, stream, static_cast<const int32_t*>(px), N, static_cast<int>(c.Hp),
-                  static_cast<int>(c.Wp), static_cast<int>(c.P), static_cast<int>(c.Q), R, S,
-                  stride_h, stride_w, rx);
-  if (rc != IGC_OK) return rc;
+  // 3. window sums of the im2col rows: for small windows the GEMM's epilogue
+  //    sums the pixel sums itself (R*S loads per output row, from L2)
+  const bool sums_in_epilogue = R * S <= kEpilogueWindowMax;
+  if (!sums_in_epilogue) {
+    rc = launch_pdl(window_sums_kernel, dim3(static_cast<unsigned>((c.M + 255) / 256)),
+                    dim3(256), 0, stream, static_cast<const int32_t*>(px), N,
+                    static_cast<int>(c.Hp), static_cast<int>(c.Wp), static_cast<int>(c.P),
+                    static_cast<int>(c.Q), R, S, stride_h, stride_w, rx);
+    if (rc != IGC_OK) return rc;
+  }
 
   // 4. the implicit GEMM over the padded tensor (no padding left for TMA)
   CUtensorMap tmA;
@@ -312,6 +333,12 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
   p.c8 = y8;
   p.ldc8 = K;
   p.rsumA = rx;
+  if (sums_in_epilogue) {
+    p.px = px;
+    p.conv_R = R;
+    p.conv_Hp = static_cast<int>(c.Hp);
+    p.conv_Wp = static_cast<int>(c.Wp);
+  }
   p.csumB = cw;
   p.zA = zX;
   p.zA_row = nullptr;

@@ -133,6 +133,11 @@ struct KParams {
   int chunk_kb;  // k-blocks per accumulation chunk (an accumulator hand-off after each)
   int conv_P, conv_Q, conv_cblocks, conv_S, conv_C;
   int pad_h, pad_w, stride_h, stride_w;
+  // integer convolution: when px is set, the row sums of the implicit im2col
+  // matrix are the sums of px (per padded pixel, conv_Hp x conv_Wp per image)
+  // over each output pixel's conv_R x conv_S window, taken in the epilogue
+  const int32_t* px;
+  int conv_R, conv_Hp, conv_Wp;
   void* out;
   long long ldo;
   int out_type;  // kOutF32 / kOutF16 / kOutBF16
@@ -429,7 +434,23 @@ __device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
   const int mm = m < p.M ? m : p.M - 1;  // rows past M are computed (and clipped) like row M-1
   IntRow r;
   r.zAp = static_cast<uint32_t>((p.zA_row ? __ldg(p.zA_row + mm) : p.zA) - p.oA);
-  r.u = static_cast<uint32_t>(__ldg(p.rsumA + mm)) - static_cast<uint32_t>(p.K) * r.zAp;
+  uint32_t rs;
+  if (p.px != nullptr) {
+    const int PQ = p.conv_P * p.conv_Q;
+    const int n = mm / PQ;
+    const int rem = mm - n * PQ;
+    const int pp = rem / p.conv_Q;
+    const int qq = rem - pp * p.conv_Q;
+    const int32_t* base = p.px + (static_cast<size_t>(n) * p.conv_Hp + static_cast<size_t>(pp) *
+                                  p.stride_h) * p.conv_Wp + static_cast<size_t>(qq) * p.stride_w;
+    rs = 0;
+    for (int r = 0; r < p.conv_R; ++r)
+      for (int s = 0; s < p.conv_S; ++s)
+        rs += static_cast<uint32_t>(__ldg(base + static_cast<size_t>(r) * p.conv_Wp + s));
+  } else {
+    rs = static_cast<uint32_t>(__ldg(p.rsumA + mm));
+  }
+  r.u = rs - static_cast<uint32_t>(p.K) * r.zAp;
   r.t_uniform = static_cast<uint32_t>(p.zB - p.oB) * r.u;
   r.sA = p.dq_row ? __ldg(p.dq_row + mm) : 1.0f;
   return r;

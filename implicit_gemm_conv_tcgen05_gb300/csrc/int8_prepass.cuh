@@ -56,30 +56,12 @@ static __device__ __forceinline__ void widen4(uint32_t word, uint32_t flip, uint
 }
 
 // One warp per row: dst[row, k] = fp16(src[row, k] - offset) for k < K, 0 for
-// K <= k < Kp; sums[row] = sum_k (src[row, k] - offset).  Both operands of a
-// GEMM go through one launch.
-static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const PrepassParams pp) {
-  grid_dependency_wait();
-  grid_dependents_launch();
-  int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
-  const int lane = static_cast<int>(threadIdx.x % 32);
-  // select the operand field by field (a dynamic index into the parameter
-  // struct would copy it to local memory)
-  const bool second = row >= pp.op[0].rows;
-  PrepassOperand o;
-  o.src = second ? pp.op[1].src : pp.op[0].src;
-  o.ld = second ? pp.op[1].ld : pp.op[0].ld;
-  o.rows = second ? pp.op[1].rows : pp.op[0].rows;
-  o.is_signed = second ? pp.op[1].is_signed : pp.op[0].is_signed;
-  o.offset = second ? pp.op[1].offset : pp.op[0].offset;
-  o.vec = second ? pp.op[1].vec : pp.op[0].vec;
-  o.dst = second ? pp.op[1].dst : pp.op[0].dst;
-  o.sums = second ? pp.op[1].sums : pp.op[0].sums;
-  if (second) row -= pp.op[0].rows;
-  if (row >= o.rows) return;
+// K <= k < Kp; sums[row] = sum_k (src[row, k] - offset).  Every lane of the
+// warp must call it (the row sum is reduced by shuffles).
+static __device__ __forceinline__ void widen_row(const PrepassOperand& o, int row, int K, int Kp,
+                                                 int lane) {
   const uint8_t* s = o.src + static_cast<size_t>(row) * o.ld;
-  __half* d = o.dst + static_cast<size_t>(row) * pp.Kp;
-  const int K = pp.K;
+  __half* d = o.dst + static_cast<size_t>(row) * Kp;
   int32_t acc = 0;
   if (o.vec) {
     // offset 128 (uint8) keeps the byte, offset 0 (int8) flips its top bit
@@ -109,7 +91,7 @@ static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const Pr
     const uint32_t nbytes = K > lane * 16 ? 16u * static_cast<uint32_t>((K - lane * 16 + 511) / 512) : 0u;
     acc = static_cast<int32_t>(usum - 128u * nbytes);
   } else {
-    for (int k = lane; k < pp.Kp; k += 32) {
+    for (int k = lane; k < Kp; k += 32) {
       int v = 0;
       if (k < K) v = shifted_byte(s[k], o.is_signed, o.offset);
       acc += v;
@@ -119,6 +101,29 @@ static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const Pr
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) o.sums[row] = acc;
+}
+
+// Both operands of a GEMM go through one launch: rows of op[0], then of op[1].
+static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const PrepassParams pp) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
+  const int lane = static_cast<int>(threadIdx.x % 32);
+  // select the operand field by field (a dynamic index into the parameter
+  // struct would copy it to local memory)
+  const bool second = row >= pp.op[0].rows;
+  PrepassOperand o;
+  o.src = second ? pp.op[1].src : pp.op[0].src;
+  o.ld = second ? pp.op[1].ld : pp.op[0].ld;
+  o.rows = second ? pp.op[1].rows : pp.op[0].rows;
+  o.is_signed = second ? pp.op[1].is_signed : pp.op[0].is_signed;
+  o.offset = second ? pp.op[1].offset : pp.op[0].offset;
+  o.vec = second ? pp.op[1].vec : pp.op[0].vec;
+  o.dst = second ? pp.op[1].dst : pp.op[0].dst;
+  o.sums = second ? pp.op[1].sums : pp.op[0].sums;
+  if (second) row -= pp.op[0].rows;
+  if (row >= o.rows) return;
+  widen_row(o, row, pp.K, pp.Kp, lane);
 }
 
 inline PrepassOperand prepass_operand(const void* src, long long ld, long long rows, long long K,

@@ -30,6 +30,7 @@ def _data(N, H, W, C, K, R, S, x_signed, w_signed, seed):
     (4, 6, 6, 128, 96, 3, 3, (0, 0), (1, 1), (0, 1)),      # no padding
     (2, 6, 7, 64, 48, 3, 3, (1, 1), (1, 1), (1, 1)),       # int8 input, 4 chunks per pixel
     (1, 5, 5, 512, 32, 3, 3, (1, 1), (1, 1), (1, 0)),      # int8 input, 32 chunks per pixel
+    (2, 9, 10, 16, 40, 7, 7, (3, 3), (1, 2), (0, 1)),      # 7x7: window sums by their own pass
 ])
 def test_conv_s8_parity(N, H, W, C, K, R, S, pad, stride, signs):
     x, w, rng = _data(N, H, W, C, K, R, S, *signs, seed=N * 100 + C + K)
