@@ -49,6 +49,8 @@ def library_path() -> str:
 def lib() -> ctypes.CDLL:
     """The loaded libigc.so (built in-tree on first use if out of date)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             from . import build as _b
@@ -121,14 +123,18 @@ def declared_functions() -> list[str]:
 # ---------------------------------------------------------------------------
 
 def _stream(stream):
+    """The cudaStream_t handle (as an int) of `stream`, or of the current stream."""
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _check(rc: int, what: str):
