@@ -681,6 +681,7 @@ template <Mode kMode, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     igc_tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmBh,
                        const __grid_constant__ CUtensorMap tmO0,
                        const __grid_constant__ CUtensorMap tmO1,
                        const __grid_constant__ CUtensorMap tmO2, const KParams p) {
@@ -726,6 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmBh);
   }
   if (warp == 1) {
     tmem_alloc_2cta(tmem_slot, Cfg::kTmemCols);
@@ -761,10 +763,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = unit_coords(p, u);
       const int mb = w.mb;
       const int m_cta = mb * BM + static_cast<int>(rank) * BM_CTA;
-      // each CTA holds half of the unit's B rows at the start of its stage buffer
-      // (a half unit uses the first BN/4 of the BN/2 rows the box brings in)
+      // each CTA holds half of the unit's B rows at the start of its stage buffer;
+      // a half unit's BN/4 rows come through tmBh, whose box is BN/4 rows
       const int n_cta = w.half ? w.nb * BN + w.j * (BN / 2) + static_cast<int>(rank) * (BN / 4)
                                : w.nb * BN + static_cast<int>(rank) * Cfg::kBNHalf;
+      const CUtensorMap* mapB = w.half ? &tmBh : &tmB;
+      const uint32_t stage_tx =
+          2u * (kStageABytes + (w.half ? Cfg::kStageBBytes / 2 : Cfg::kStageBBytes));
       int cn = 0, ch = 0, cw = 0;
       if constexpr (mode_is_conv(kMode)) {
         const int PQ = p.conv_P * p.conv_Q;
@@ -783,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* a_dst = sA + stage * kStageABytes;
           uint8_t* b_dst = sB + stage * Cfg::kStageBBytes;
           const uint32_t bar = full_lead + static_cast<uint32_t>(stage) * 8u;
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * Cfg::kStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
           if constexpr (mode_is_conv(kMode)) {
             const int tap = kb / p.conv_cblocks;
             const int c0 = (kb - tap * p.conv_cblocks) * KS;
@@ -793,14 +798,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < kAtoms; ++j) {
               tma_load_im2col_4d_2cta(a_dst + j * kAtomABytes, &tmA, bar, c0 + j * BK, cw, ch, cn,
                                       static_cast<uint16_t>(s), static_cast<uint16_t>(r));
-              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, &tmB, bar,
+              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, mapB, bar,
                                tap * p.conv_C + c0 + j * BK, n_cta);
             }
           } else {
 #pragma unroll
             for (int j = 0; j < kAtoms; ++j) {
               tma_load_2d_2cta(a_dst + j * kAtomABytes, &tmA, bar, kb * KS + j * BK, m_cta);
-              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, &tmB, bar, kb * KS + j * BK, n_cta);
+              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, mapB, bar, kb * KS + j * BK, n_cta);
             }
           }
         }

@@ -96,7 +96,7 @@ inline void add_out_map(OutMaps& o, int slot, CUtensorMapDataType dtype, const v
 
 template <Mode kMode, int BN>
 int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                   const OutMaps& om, KParams p, cudaStream_t stream) {
+                   const CUtensorMap& tmBh, const OutMaps& om, KParams p, cudaStream_t stream) {
   int max_clusters = 0;
   int rc = kernel_setup<kMode, BN>(dev, &max_clusters);
   if (rc != IGC_OK) return rc;
@@ -130,7 +130,7 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN>, tmA, tmB, om.map[0],
+  if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN>, tmA, tmB, tmBh, om.map[0],
                          om.map[1], om.map[2], p) != cudaSuccess) {
     (void)cudaGetLastError();
     return IGC_ERR_CUDA;
@@ -172,8 +172,9 @@ constexpr double kBnEff[] = {1.0, 0.97, 0.87};
 constexpr int kBnCandsInt[] = {256, 128};
 constexpr double kBnEffInt[] = {1.0, 0.87};
 
-// Picks the tile width for this problem, encodes B's tensor map with a box of
-// BN/2 rows (each CTA of the pair loads half of the B tile) and launches.
+// Picks the tile width for this problem, encodes B's tensor maps with boxes of
+// BN/2 rows (each CTA of the pair loads half of the B tile) and BN/4 rows (half
+// of a column-half unit's B) and launches.
 template <Mode kMode>
 int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_base,
                    uint64_t b_inner, uint64_t b_rows, uint64_t b_row_bytes, const OutMaps& om,
@@ -188,15 +189,18 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
                               : pick_bn(p.M, p.N, clusters, kBnCands, kBnEff, 3);
   const int forced = tile_width_override();
   if (forced == 256 || forced == 128 || (forced == 224 && !mode_is_int(kMode))) bn = forced;
-  CUtensorMap tmB;
+  CUtensorMap tmB, tmBh;  // boxes of BN/2 rows (whole tiles) and BN/4 rows (column halves)
   rc = encode_tiled_2d(&tmB, kBType, b_base, b_inner, b_rows,
                        b_row_bytes, BK, static_cast<uint32_t>(bn / 2));
   if (rc != IGC_OK) return rc;
+  rc = encode_tiled_2d(&tmBh, kBType, b_base, b_inner, b_rows,
+                       b_row_bytes, BK, static_cast<uint32_t>(bn / 4));
+  if (rc != IGC_OK) return rc;
   if constexpr (!mode_is_int(kMode))
-    if (bn == 224) return launch_tc_gemm<kMode, 224>(dev, tmA, tmB, om, p, stream);
+    if (bn == 224) return launch_tc_gemm<kMode, 224>(dev, tmA, tmB, tmBh, om, p, stream);
   switch (bn) {
-    case 256: return launch_tc_gemm<kMode, 256>(dev, tmA, tmB, om, p, stream);
-    case 128: return launch_tc_gemm<kMode, 128>(dev, tmA, tmB, om, p, stream);
+    case 256: return launch_tc_gemm<kMode, 256>(dev, tmA, tmB, tmBh, om, p, stream);
+    case 128: return launch_tc_gemm<kMode, 128>(dev, tmA, tmB, tmBh, om, p, stream);
     default: return IGC_ERR_UNSUPPORTED;
   }
 }
