@@ -560,8 +560,9 @@ __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMa
       }
     }
   }
-  // int32 and dequantised fp32: 32-bit values, boxes of 32 columns (two groups)
-#pragma unroll
+  // int32 and dequantised fp32: 32-bit values, boxes of 32 columns (two groups);
+  // one copy of the loop body for both outputs keeps the register count down
+#pragma unroll 1
   for (int o = 0; o < 2; ++o) {
     void* outp = o == 0 ? static_cast<void*>(p.c32) : static_cast<void*>(p.yf);
     if (outp == nullptr) continue;
