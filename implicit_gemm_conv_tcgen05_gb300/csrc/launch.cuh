@@ -68,7 +68,7 @@ int kernel_setup(const DeviceInfo& dev, int* max_clusters) {
       n = dev.sm_count / 2;  // one CTA per SM, pairs
     }
     s.max_clusters[d] = n;
-    s.rc[d] = IGC_OK;
+    s.rc[d] = n > 0 ? IGC_OK : IGC_ERR_UNSUPPORTED;
   });
   *max_clusters = s.max_clusters[d];
   return s.rc[d];
