@@ -20,7 +20,7 @@ struct PrepassOperand {
   int rows;
   int is_signed;
   int offset;
-  int vec;  // K % 16 == 0, 16-byte aligned rows: 16-byte loads
+  int vec;  // K % 16 == 0, 16-byte aligned rows: vector loads and stores
   __half* dst;
   int32_t* sums;
 };
@@ -30,7 +30,7 @@ struct PrepassParams {
   int K, Kp;
 };
 
-constexpr int kPrepassUnroll = 4;  // 16-byte loads in flight per thread
+constexpr int kPrepassUnroll = 8;  // 8-byte loads in flight per thread
 
 static __device__ __forceinline__ int shifted_byte(uint32_t byte, int is_signed, int offset) {
   return (is_signed ? static_cast<int>(static_cast<int8_t>(byte)) : static_cast<int>(byte)) -
@@ -67,28 +67,28 @@ static __device__ __forceinline__ void widen_row(const PrepassOperand& o, int ro
     // offset 128 (uint8) keeps the byte, offset 0 (int8) flips its top bit
     const uint32_t flip = o.offset == 128 ? 0u : 0x80808080u;
     uint32_t usum = 0;  // sum of the u bytes; the shifted sum is usum - 128 K
-    for (int k0 = lane * 16; k0 < K; k0 += 32 * 16 * kPrepassUnroll) {
-      uint4 raw[kPrepassUnroll];
+    // lane l reads 8 bytes at k = 8 l + 256 i and writes their 16 output bytes, so
+    // each warp-wide store covers 512 contiguous bytes
+    for (int k0 = lane * 8; k0 < K; k0 += 32 * 8 * kPrepassUnroll) {
+      uint2 raw[kPrepassUnroll];
 #pragma unroll
       for (int u = 0; u < kPrepassUnroll; ++u) {
-        const int k = k0 + u * 32 * 16;
-        raw[u] = k < K ? __ldg(reinterpret_cast<const uint4*>(s + k)) : make_uint4(0, 0, 0, 0);
+        const int k = k0 + u * 32 * 8;
+        raw[u] = k < K ? __ldg(reinterpret_cast<const uint2*>(s + k)) : make_uint2(0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kPrepassUnroll; ++u) {
-        const int k = k0 + u * 32 * 16;
+        const int k = k0 + u * 32 * 8;
         if (k >= K) break;
-        uint32_t out[8];
+        uint32_t out[4];
         widen4(raw[u].x, flip, out[0], out[1], usum);
         widen4(raw[u].y, flip, out[2], out[3], usum);
-        widen4(raw[u].z, flip, out[4], out[5], usum);
-        widen4(raw[u].w, flip, out[6], out[7], usum);
-        reinterpret_cast<uint4*>(d + k)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        reinterpret_cast<uint4*>(d + k)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        *reinterpret_cast<uint4*>(d + k) = make_uint4(out[0], out[1], out[2], out[3]);
       }
     }
-    // the lane read 16 bytes at k = 16 lane + 512 i for every such k < K
-    const uint32_t nbytes = K > lane * 16 ? 16u * static_cast<uint32_t>((K - lane * 16 + 511) / 512) : 0u;
+    // the lane read 8 bytes at k = 8 lane + 256 i for every such k < K
+    const uint32_t nbytes =
+        K > lane * 8 ? 8u * static_cast<uint32_t>((K - lane * 8 + 255) / 256) : 0u;
     acc = static_cast<int32_t>(usum - 128u * nbytes);
   } else {
     for (int k = lane; k < Kp; k += 32) {
