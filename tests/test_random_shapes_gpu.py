@@ -1,0 +1,109 @@
+"""Seeded randomized parity sweep: many shapes and parameter combinations per
+operation, each compared with the oracle (int8 bit-exact, floating point within
+the per-element bound).  Shapes are drawn so that tile widths, the split last
+round, ragged edges, strides, zero-point kinds and signedness vary together."""
+
+import numpy as np
+import pytest
+import torch
+
+import implicit_gemm_conv_tcgen05_gb300 as igc
+import oracle
+import synth
+from gpu_helpers import (assert_f16_is_rne_of_f32, assert_fp16_bound, check_device_ok, dev,
+                         host)
+
+pytestmark = pytest.mark.gpu
+
+_RNG = np.random.default_rng(20261202)
+_GEMM_F16 = [(int(_RNG.integers(1, 700)), int(_RNG.integers(1, 1300)), 8 * int(_RNG.integers(1, 160)))
+             for _ in range(16)]
+_GEMM_S8 = [(int(_RNG.integers(1, 600)), int(_RNG.integers(1, 900)), 16 * int(_RNG.integers(1, 100)),
+             int(_RNG.integers(0, 2)), int(_RNG.integers(0, 2)), int(_RNG.integers(0, 4)))
+            for _ in range(16)]
+_CONV = []
+while len(_CONV) < 12:
+    R, S = int(_RNG.integers(1, 6)), int(_RNG.integers(1, 6))
+    ph, pw = int(_RNG.integers(0, R)), int(_RNG.integers(0, S))
+    sh, sw = int(_RNG.integers(1, 4)), int(_RNG.integers(1, 4))
+    H, W = int(_RNG.integers(R, 16)), int(_RNG.integers(S, 16))
+    C = 8 * int(_RNG.integers(1, 24))
+    K = 8 * int(_RNG.integers(1, 40))
+    N = int(_RNG.integers(1, 4))
+    _CONV.append((N, H, W, C, K, R, S, (ph, pw), (sh, sw)))
+
+
+@pytest.mark.parametrize("M,N,K", _GEMM_F16)
+def test_random_gemm_f16(M, N, K):
+    A = synth.normal_f16(M * 31 + K, 1, (M, K))
+    Bt = synth.normal_f16(N * 37 + K, 2, (N, K))
+    C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    igc.gemm_f16(dev(A), dev(Bt), C, C32)
+    check_device_ok()
+    ref, sabs = oracle.gemm_f16(A, Bt)
+    c32 = host(C32)
+    assert_fp16_bound(c32, ref, sabs, f"{M}x{N}x{K}")
+    assert_f16_is_rne_of_f32(host(C), c32, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,a_signed,b_signed,zkind", _GEMM_S8)
+def test_random_gemm_s8(M, N, K, a_signed, b_signed, zkind):
+    """zkind: 0 per-tensor zero points and scale, 1 per-row zA, 2 per-column zB and
+    scale, 3 both vectors."""
+    rng = np.random.default_rng(M * 1000 + N * 7 + K)
+    A = (rng.integers(-128, 128, size=(M, K)).astype(np.int8) if a_signed
+         else rng.integers(0, 256, size=(M, K)).astype(np.uint8))
+    Bt = (rng.integers(-128, 128, size=(N, K)).astype(np.int8) if b_signed
+          else rng.integers(0, 256, size=(N, K)).astype(np.uint8))
+    lo_a, hi_a = (-128, 128) if a_signed else (0, 256)
+    lo_b, hi_b = (-128, 128) if b_signed else (0, 256)
+    kw = dict(zA=int(rng.integers(lo_a, hi_a)), zB=int(rng.integers(lo_b, hi_b)),
+              scale=float(np.float32(2.0 ** -int(rng.integers(8, 16)))))
+    if zkind in (1, 3):
+        kw["zA_row"] = rng.integers(lo_a, hi_a, size=M).astype(np.int32)
+    if zkind in (2, 3):
+        kw["zB_col"] = rng.integers(lo_b, hi_b, size=N).astype(np.int32)
+        kw["scale_col"] = synth.uniform_f32(M + N, 5, (N,), 1e-6, 1e-3)
+    C32 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    C8 = torch.empty((M, N), dtype=torch.int8, device="cuda")
+    igc.gemm_s8_zp(dev(A), dev(Bt), zA=kw["zA"], zB=kw["zB"], scale=kw["scale"],
+                   zA_row=dev(kw["zA_row"]) if "zA_row" in kw else None,
+                   zB_col=dev(kw["zB_col"]) if "zB_col" in kw else None,
+                   scale_col=dev(kw["scale_col"]) if "scale_col" in kw else None,
+                   C32=C32, C8=C8)
+    check_device_ok()
+    o32, o8, _, _ = oracle.gemm_s8_zp(A, Bt, a_signed=a_signed, b_signed=b_signed, **kw)
+    assert np.array_equal(host(C32), o32)
+    assert np.array_equal(host(C8), o8)
+
+
+@pytest.mark.parametrize("N,H,W,C,K,R,S,pad,stride", _CONV)
+def test_random_conv_f16_and_s8(N, H, W, C, K, R, S, pad, stride):
+    x = synth.normal_f16(N * 100 + C, 6, (N, H, W, C))
+    w = synth.normal_f16(K * 100 + R * 10 + S, 7, (K, R, S, C), std=1.0 / np.sqrt(R * S * C))
+    P = (H + 2 * pad[0] - R) // stride[0] + 1
+    Q = (W + 2 * pad[1] - S) // stride[1] + 1
+    y = torch.empty((N, P, Q, K), dtype=torch.float16, device="cuda")
+    y32 = torch.empty((N, P, Q, K), dtype=torch.float32, device="cuda")
+    igc.conv2d_nhwc_f16_implicit(dev(x), dev(w), y, y32, pad=pad, stride=stride)
+    check_device_ok()
+    ref, sabs = oracle.conv2d_nhwc_f16(x, w, pad=pad, stride=stride)
+    assert_fp16_bound(host(y32), ref, sabs, "conv f16")
+    assert_f16_is_rne_of_f32(host(y), host(y32), "conv f16")
+
+    rng = np.random.default_rng(N * 7 + C + K)
+    x8 = rng.integers(0, 256, size=(N, H, W, C)).astype(np.uint8)
+    w8 = rng.integers(-128, 128, size=(K, R, S, C)).astype(np.int8)
+    zX = int(rng.integers(0, 256))
+    zW_k = rng.integers(-30, 30, size=K).astype(np.int32)
+    scale_k = rng.uniform(1e-5, 1e-3, size=K).astype(np.float32)
+    g32 = torch.empty((N, P, Q, K), dtype=torch.int32, device="cuda")
+    g8 = torch.empty((N, P, Q, K), dtype=torch.int8, device="cuda")
+    igc.conv2d_nhwc_s8_zp(dev(x8), dev(w8), zX, zW_k=dev(zW_k), y32=g32, y8=g8,
+                          scale_k=dev(scale_k), pad=pad, stride=stride)
+    check_device_ok()
+    o32, o8, _ = oracle.conv2d_nhwc_s8_zp(x8, w8, x_signed=0, w_signed=1, zX=zX, zW_k=zW_k,
+                                          pad=pad, stride=stride, scale_k=scale_k)
+    assert np.array_equal(host(g32), o32)
+    assert np.array_equal(host(g8), o8)
