@@ -110,6 +110,15 @@ struct TileCfg {
   // column of accumulator 1 (a multiple of 32, so every tcgen05.ld starts aligned)
   static constexpr uint32_t kAccStride = kTmemCols / 2;
   static constexpr int kEpiCols = BN / 2;  // columns per epilogue warp
+  // Column-half units take A 32 KB + B 16 KB per stage and use them up in half the
+  // MMA time of a whole tile's stage, so with three stages the copies in flight
+  // cover half the time.  At BN = 256 the last round therefore switches to a ring
+  // of four such 48 KB stages laid over the memory of the three 64 KB ones
+  // (tail_slot); slot i is filled only once the main stages whose memory it
+  // reuses have been released.
+  static constexpr bool kTailRing = BN == 256 && kStages == 3;
+  static constexpr int kTailStages = 4;
+  static_assert(!kTailRing || (kStageABytes == 32768 && kStageBBytes == 32768), "tail ring");
 };
 
 // wait sites, reported in the device status word
@@ -121,6 +130,50 @@ enum : uint32_t {
   kSiteDrain = 5,
   kSiteTmemMismatch = 6,
 };
+
+// Tail-ring slot `i` (BN = 256) after the switch from the main ring, whose stages
+// lie at A: 32K s and B: 96K + 32K s and whose oldest stage (the first the MMAs
+// release) is m0; m1, m2 follow in release order.  Byte offsets of the slot's A
+// (32 KB) and B (16 KB) parts:
+//   slot 0: A(m0), B(m0) low half     slot 1: A(m1), B(m0) high half
+//   slot 2: B(m1), B(m2) low half     slot 3: A(m2), B(m2) high half
+// Slot i's first fill therefore needs main stages m0..m_min(i,2) released, in order.
+__device__ __forceinline__ void tail_slot(int i, int m0, uint32_t& a_off, uint32_t& b_off) {
+  constexpr uint32_t kS = 32768u, kB0 = 3u * 32768u, kHalfB = 16384u;
+  const uint32_t m1 = m0 == 2 ? 0u : static_cast<uint32_t>(m0) + 1u;
+  const uint32_t m2 = m1 == 2u ? 0u : m1 + 1u;
+  const uint32_t s0 = static_cast<uint32_t>(m0);
+  if (i == 0) {
+    a_off = s0 * kS;
+    b_off = kB0 + s0 * kS;
+  } else if (i == 1) {
+    a_off = m1 * kS;
+    b_off = kB0 + s0 * kS + kHalfB;
+  } else if (i == 2) {
+    a_off = kB0 + m1 * kS;
+    b_off = kB0 + m2 * kS;
+  } else {
+    a_off = m2 * kS;
+    b_off = kB0 + m2 * kS + kHalfB;
+  }
+}
+
+// Leader CTA, after an abort: waits (briefly) for the last fills of a ring whose
+// next fill would be `stage` in `phase`, so that no copy is still landing when the
+// CTA exits.
+__device__ __forceinline__ void drain_fills(uint64_t* full_arr, int n, int stage, uint32_t phase,
+                                            long long issued, uint64_t lim) {
+  int s = stage;
+  uint32_t ph = phase;
+  for (long long i = 0; i < issued && i < n; ++i) {
+    if (--s < 0) {
+      s = n - 1;
+      ph ^= 1u;
+    }
+    int dummy = 0;
+    mbar_wait(&full_arr[s], ph, lim / 64 + 1000, &dummy, nullptr, kSiteDrain);
+  }
+}
 
 struct KParams {
   int M, N, K;
@@ -202,6 +255,52 @@ __device__ __forceinline__ Unit unit_coords(const KParams& p, int u) {
   }
   tile_coords(p, t, w.mb, w.nb);
   return w;
+}
+
+// One pipeline stage's TMA copies into a_dst / b_dst: kAtoms swizzle atoms of A
+// (kAtomABytes apart) and of B (kBAtom apart), all completing on barrier `bar`
+// of the leader CTA.  A convolution's stage kb is channel block kb % cblocks of
+// filter tap kb / cblocks, its A rows gathered by TMA im2col.
+template <Mode kMode, uint32_t kBAtom>
+__device__ __forceinline__ void load_stage(const KParams& p, const CUtensorMap* tmA,
+                                           const CUtensorMap* mapB, uint8_t* a_dst, uint8_t* b_dst,
+                                           uint32_t bar, int kb, int m_cta, int n_cta, int cn,
+                                           int ch, int cw) {
+  if constexpr (mode_is_conv(kMode)) {
+    const int tap = kb / p.conv_cblocks;
+    const int c0 = (kb - tap * p.conv_cblocks) * KS;
+    const int r = tap / p.conv_S;
+    const int s = tap - r * p.conv_S;
+#pragma unroll
+    for (int j = 0; j < kAtoms; ++j) {
+      tma_load_im2col_4d_2cta(a_dst + j * kAtomABytes, tmA, bar, c0 + j * BK, cw, ch, cn,
+                              static_cast<uint16_t>(s), static_cast<uint16_t>(r));
+      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, tap * p.conv_C + c0 + j * BK, n_cta);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kAtoms; ++j) {
+      tma_load_2d_2cta(a_dst + j * kAtomABytes, tmA, bar, kb * KS + j * BK, m_cta);
+      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, kb * KS + j * BK, n_cta);
+    }
+  }
+}
+
+// One pipeline stage's MMAs (kAtoms atoms x BK/16 steps of k = 16) into the
+// accumulator at d_tmem; a_st / b_st are the stage's first descriptors, B atoms
+// lie kBAtom apart.  The first MMA of a chunk overwrites the accumulator.
+template <uint32_t kBAtom>
+__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint64_t a_st, uint64_t b_st,
+                                          uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int j = 0; j < kAtoms; ++j) {
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      const uint64_t ad = a_st + ((j * kAtomABytes + k * 32) >> 4);
+      const uint64_t bd = b_st + ((j * kBAtom + k * 32) >> 4);
+      umma_f16_ss_2cta(d_tmem, ad, bd, idesc, (accumulate || j > 0 || k > 0) ? 1u : 0u);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -703,7 +802,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = bars + 2 * kStages;  // each CTA: accumulator a is ready
   uint64_t* tempty = tfull + 2;          // leader: both epilogues released accumulator a
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* full_t = mma_done + 1;                // tail ring (Cfg::kTailRing)
+  uint64_t* empty_t = full_t + Cfg::kTailStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_t + Cfg::kTailStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
@@ -722,6 +823,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[a], 2 * kEpiWarps);
     }
     mbar_init(mma_done, 1);
+    if constexpr (Cfg::kTailRing) {
+      for (int s = 0; s < Cfg::kTailStages; ++s) {
+        mbar_init(&full_t[s], 1);
+        mbar_init(&empty_t[s], 1);
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -750,6 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!pair_ok && threadIdx.x == 0) report_status(p.status, kStatusBadLaunch, kSiteTmemMismatch);
   // the leader's barriers, as cluster addresses usable from either CTA
   const uint32_t full_lead = mapa_shared(smem_u32(full), 0);
+  const uint32_t full_t_lead = mapa_shared(smem_u32(full_t), 0);
   const uint32_t tempty_lead = mapa_shared(smem_u32(tempty), 0);
 
   if (warp < 4) {
@@ -760,6 +868,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
+    // tail ring: the main ring's next stage and phase at the switch (sw_stage >= 0
+    // once switched) and the fills issued on the main ring before it
+    int sw_stage = -1;
+    uint32_t sw_phase = 0;
+    long long issued_main = 0;
     for (int u = cluster; u < p.num_units; u += num_clusters) {
       const Unit w = unit_coords(p, u);
       const int mb = w.mb;
@@ -781,57 +894,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         ch = pp * p.stride_h - p.pad_h;
         cw = qq * p.stride_w - p.pad_w;
       }
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, lim, abort_flag,
-                                                p.status, kSiteProducerEmpty)))
-          goto producer_done;
-        if (lane == 0) {
-          uint8_t* a_dst = sA + stage * kStageABytes;
-          uint8_t* b_dst = sB + stage * Cfg::kStageBBytes;
-          const uint32_t bar = full_lead + static_cast<uint32_t>(stage) * 8u;
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
-          if constexpr (mode_is_conv(kMode)) {
-            const int tap = kb / p.conv_cblocks;
-            const int c0 = (kb - tap * p.conv_cblocks) * KS;
-            const int r = tap / p.conv_S;
-            const int s = tap - r * p.conv_S;
-#pragma unroll
-            for (int j = 0; j < kAtoms; ++j) {
-              tma_load_im2col_4d_2cta(a_dst + j * kAtomABytes, &tmA, bar, c0 + j * BK, cw, ch, cn,
-                                      static_cast<uint16_t>(s), static_cast<uint16_t>(r));
-              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, mapB, bar,
-                               tap * p.conv_C + c0 + j * BK, n_cta);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < kAtoms; ++j) {
-              tma_load_2d_2cta(a_dst + j * kAtomABytes, &tmA, bar, kb * KS + j * BK, m_cta);
-              tma_load_2d_2cta(b_dst + j * Cfg::kAtomBBytes, mapB, bar, kb * KS + j * BK, n_cta);
-            }
+      if (!Cfg::kTailRing || !w.half) {
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, lim, abort_flag,
+                                                  p.status, kSiteProducerEmpty)))
+            goto producer_done;
+          if (lane == 0) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
+            load_stage<kMode, Cfg::kAtomBBytes>(p, &tmA, mapB, sA + stage * kStageABytes,
+                                                sB + stage * Cfg::kStageBBytes,
+                                                full_lead + static_cast<uint32_t>(stage) * 8u, kb,
+                                                m_cta, n_cta, cn, ch, cw);
+          }
+          __syncwarp();
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        __syncwarp();
-        ++issued;
-        if (++stage == kStages) {
+      } else if constexpr (Cfg::kTailRing) {
+        if (sw_stage < 0) {
+          sw_stage = stage;
+          sw_phase = phase;
+          issued_main = issued;
           stage = 0;
-          phase ^= 1u;
+          phase = 0;
+          issued = 0;
+        }
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty_t[stage], phase ^ 1u, lim, abort_flag,
+                                                  p.status, kSiteProducerEmpty)))
+            goto producer_done;
+          if (issued < kStages) {
+            // first fill of tail slot `issued`: main stage m_issued (released after
+            // m_0 .. m_issued-1, which earlier fills waited for) must be free
+            const int ms = (sw_stage + static_cast<int>(issued)) % kStages;
+            const uint32_t par = ms < sw_stage ? sw_phase : (sw_phase ^ 1u);
+            if (!__all_sync(0xffffffffu, mbar_wait(&empty[ms], par, lim, abort_flag, p.status,
+                                                    kSiteProducerEmpty)))
+              goto producer_done;
+          }
+          if (lane == 0) {
+            uint32_t a_off, b_off;
+            tail_slot(stage, sw_stage, a_off, b_off);
+            if (rank == 0) mbar_arrive_expect_tx(&full_t[stage], stage_tx);
+            load_stage<kMode, Cfg::kAtomBBytes / 2>(p, &tmA, mapB, smem + a_off, smem + b_off,
+                                                    full_t_lead + static_cast<uint32_t>(stage) * 8u,
+                                                    kb, m_cta, n_cta, cn, ch, cw);
+          }
+          __syncwarp();
+          ++issued;
+          if (++stage == Cfg::kTailStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
   producer_done:
-    if (lane == 0 && *abort_flag && issued > 0) {
+    if (lane == 0 && *abort_flag && (issued > 0 || issued_main > 0)) {
       // The copies signal the leader's barriers; give this CTA's own in-flight
       // copies time to land before the CTA may exit (a copy takes microseconds).
       if (rank == 0) {
-        int s = stage;
-        uint32_t ph = phase;
-        for (long long i = 0; i < issued && i < kStages; ++i) {
-          if (--s < 0) {
-            s = kStages - 1;
-            ph ^= 1u;
-          }
-          int dummy = 0;
-          mbar_wait(&full[s], ph, lim / 64 + 1000, &dummy, nullptr, kSiteDrain);
+        if (sw_stage >= 0) {
+          drain_fills(full_t, Cfg::kTailStages, stage, phase, issued, lim);
+          drain_fills(full, kStages, sw_stage, sw_phase, issued_main, lim);
+        } else {
+          drain_fills(full, kStages, stage, phase, issued, lim);
         }
       } else {
         const uint64_t t0 = globaltimer_ns();
@@ -855,46 +985,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int sw_stage = -1;  // main-ring stage at the switch to the tail ring
       for (int u = cluster; u < p.num_units; u += num_clusters) {
-        const uint32_t idesc = u >= p.tail_start ? idesc_half : idesc_full;
+        const bool half_unit = u >= p.tail_start;
+        const uint32_t idesc = half_unit ? idesc_half : idesc_full;
         int kin = 0;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (kin == 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, lim, abort_flag,
-                                                    p.status, kSiteMmaTmemEmpty)))
+        if (!Cfg::kTailRing || !half_unit) {
+          for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (kin == 0) {
+              if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, lim,
+                                                      abort_flag, p.status, kSiteMmaTmemEmpty)))
+                goto mma_done_label;
+              tc_fence_after();
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, lim, abort_flag, p.status,
+                                                    kSiteMmaFull)))
               goto mma_done_label;
             tc_fence_after();
-          }
-          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, lim, abort_flag, p.status,
-                                                  kSiteMmaFull)))
-            goto mma_done_label;
-          tc_fence_after();
-          const bool chunk_end = (kin == p.chunk_kb - 1) || (kb == p.num_kb - 1);
-          if (lane == 0) {
-            const uint64_t a_st = adesc0 + ((static_cast<uint32_t>(stage) * kStageABytes) >> 4);
-            const uint64_t b_st = bdesc0 + ((static_cast<uint32_t>(stage) * Cfg::kStageBBytes) >> 4);
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * Cfg::kAccStride;
-#pragma unroll
-            for (int j = 0; j < kAtoms; ++j) {
-#pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                const uint64_t ad = a_st + ((j * kAtomABytes + k * 32) >> 4);
-                const uint64_t bd = b_st + ((j * Cfg::kAtomBBytes + k * 32) >> 4);
-                umma_f16_ss_2cta(d_tmem, ad, bd, idesc, (kin > 0 || j > 0 || k > 0) ? 1u : 0u);
-              }
+            const bool chunk_end = (kin == p.chunk_kb - 1) || (kb == p.num_kb - 1);
+            if (lane == 0) {
+              mma_stage<Cfg::kAtomBBytes>(
+                  tmem_base + static_cast<uint32_t>(acc) * Cfg::kAccStride,
+                  adesc0 + ((static_cast<uint32_t>(stage) * kStageABytes) >> 4),
+                  bdesc0 + ((static_cast<uint32_t>(stage) * Cfg::kStageBBytes) >> 4), idesc,
+                  kin > 0);
+              umma_commit_2cta_multicast(&empty[stage], 0x3);
+              if (chunk_end) umma_commit_2cta_multicast(&tfull[acc], 0x3);
             }
-            umma_commit_2cta_multicast(&empty[stage], 0x3);
-            if (chunk_end) umma_commit_2cta_multicast(&tfull[acc], 0x3);
+            __syncwarp();
+            if (chunk_end) {
+              acc ^= 1;
+              if (acc == 0) acc_phase ^= 1u;
+            }
+            if (++kin == p.chunk_kb) kin = 0;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          __syncwarp();
-          if (chunk_end) {
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
-          }
-          if (++kin == p.chunk_kb) kin = 0;
-          if (++stage == kStages) {
+        } else if constexpr (Cfg::kTailRing) {
+          if (sw_stage < 0) {
+            sw_stage = stage;
             stage = 0;
-            phase ^= 1u;
+            phase = 0;
+          }
+          for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (kin == 0) {
+              if (!__all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1u, lim,
+                                                      abort_flag, p.status, kSiteMmaTmemEmpty)))
+                goto mma_done_label;
+              tc_fence_after();
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(&full_t[stage], phase, lim, abort_flag,
+                                                    p.status, kSiteMmaFull)))
+              goto mma_done_label;
+            tc_fence_after();
+            const bool chunk_end = (kin == p.chunk_kb - 1) || (kb == p.num_kb - 1);
+            if (lane == 0) {
+              // the rings share their base, sA, whose descriptor is adesc0
+              uint32_t a_off, b_off;
+              tail_slot(stage, sw_stage, a_off, b_off);
+              mma_stage<Cfg::kAtomBBytes / 2>(
+                  tmem_base + static_cast<uint32_t>(acc) * Cfg::kAccStride, adesc0 + (a_off >> 4),
+                  adesc0 + (b_off >> 4), idesc, kin > 0);
+              umma_commit_2cta_multicast(&empty_t[stage], 0x3);
+              if (chunk_end) umma_commit_2cta_multicast(&tfull[acc], 0x3);
+            }
+            __syncwarp();
+            if (chunk_end) {
+              acc ^= 1;
+              if (acc == 0) acc_phase ^= 1u;
+            }
+            if (++kin == p.chunk_kb) kin = 0;
+            if (++stage == Cfg::kTailStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
