@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
             L.igc_set_wait_limit_ns.restype = ctypes.c_uint64
             L.igc_set_tile_width.argtypes = [i32]
             L.igc_set_tile_width.restype = i32
+            L.igc_set_stage_depth.argtypes = [i32]
+            L.igc_set_stage_depth.restype = i32
             L.igc_debug_wait_timeout_probe.argtypes = [vp]
             L.igc_debug_wait_timeout_probe.restype = i32
             L.igc_version.argtypes = []
@@ -171,6 +173,10 @@ def igc_last_device_status() -> int:
 
 def igc_set_tile_width(bn: int) -> int:
     return int(lib().igc_set_tile_width(int(bn)))
+
+
+def igc_set_stage_depth(k: int) -> int:
+    return int(lib().igc_set_stage_depth(int(k)))
 
 
 def igc_set_wait_limit_ns(limit_ns: int) -> int:

@@ -19,6 +19,7 @@ __device__ unsigned long long g_status_word;
 
 std::atomic<unsigned long long> g_wait_limit{2000000000ull};
 std::atomic<int> g_tile_width{0};  // 0: chosen per problem
+std::atomic<int> g_stage_depth{0};  // 0: chosen per problem
 std::atomic<unsigned long long> g_last_status{0};
 
 struct DeviceSlot {
@@ -120,6 +121,8 @@ unsigned long long wait_limit_ns() { return g_wait_limit.load(); }
 
 int tile_width_override() { return g_tile_width.load(); }
 
+int stage_depth_override() { return g_stage_depth.load(); }
+
 int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                     uint32_t box_rows) {
@@ -199,6 +202,11 @@ uint64_t igc_last_device_status(void) { return igc::g_last_status.load(); }
 int igc_set_tile_width(int bn) {
   if (bn != 0 && bn != 128 && bn != 224 && bn != 256) return -1;
   return igc::g_tile_width.exchange(bn);
+}
+
+int igc_set_stage_depth(int k) {
+  if (k != 0 && k != 64 && k != 128) return -1;
+  return igc::g_stage_depth.exchange(k);
 }
 
 uint64_t igc_set_wait_limit_ns(uint64_t limit_ns) {

@@ -70,8 +70,8 @@ enum : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 constexpr int BM = 256;        // rows per cluster tile (128 per CTA)
 constexpr int BM_CTA = 128;
 constexpr int BK = 64;         // 64 fp16 = one 128-byte swizzle row (one TMA box, one atom)
-constexpr int kAtoms = 2;      // swizzle atoms along k per pipeline stage
-constexpr int KS = BK * kAtoms;  // k depth of one pipeline stage (8 MMAs of k = 16)
+constexpr int kAtoms = 2;      // swizzle atoms along k per pipeline stage (default)
+constexpr int KS = BK * kAtoms;  // k depth of one default pipeline stage (8 MMAs of k = 16)
 constexpr int kEpiWarps = 8;
 // Three warpgroups: warps 0-3 (TMA producer, MMA issuer / TMEM owner, two idle)
 // and two epilogue warpgroups (warps 4-11).  After set-up the first warpgroup
@@ -84,7 +84,6 @@ constexpr int kRegsHigh = 216;
 constexpr int kMinLaunchRegs = 168;
 static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kThreads * kMinLaunchRegs, "register split");
 constexpr uint32_t kAtomABytes = BM_CTA * BK * 2;   // 16 KB
-constexpr uint32_t kStageABytes = kAtomABytes * kAtoms;
 constexpr uint32_t kBarrierBytes = 512;
 // Each epilogue warp stages 32 rows x 128 bytes of output in shared memory (128-byte
 // swizzle, the layout of a TMA box) and writes them with one bulk tensor store.
@@ -93,12 +92,19 @@ constexpr uint32_t kStagingBytes = kEpiWarps * kStagingWarpBytes;
 constexpr size_t kSmemBudget = 227 * 1024;
 constexpr int kIntChunkKb = 1024 / KS;  // stages per exact fp32 accumulation chunk (1024 k)
 
-template <int BN>
+// ATOMS: swizzle atoms along k per pipeline stage.  The default, 2 (128-deep
+// stages, 8 MMAs each), has the least per-stage overhead; 1 (64-deep stages,
+// about twice as many) keeps more of the ring in flight, which pays for shapes
+// that run one or two rounds and stream their operands from DRAM.
+template <int BN, int ATOMS = kAtoms>
 struct TileCfg {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(ATOMS == 1 || ATOMS == 2, "ATOMS");
+  static constexpr int kKS = BK * ATOMS;                        // k depth of a stage
+  static constexpr uint32_t kStageABytes = kAtomABytes * ATOMS;
   static constexpr int kBNHalf = BN / 2;                        // B rows per CTA
   static constexpr uint32_t kAtomBBytes = kBNHalf * BK * 2;
-  static constexpr uint32_t kStageBBytes = kAtomBBytes * kAtoms;
+  static constexpr uint32_t kStageBBytes = kAtomBBytes * ATOMS;
   static constexpr uint32_t kStageBytes = kStageABytes + kStageBBytes;
   static constexpr int kStages =
       static_cast<int>((kSmemBudget - 1024 - kBarrierBytes - kStagingBytes) / kStageBytes) > 8
@@ -257,43 +263,44 @@ __device__ __forceinline__ Unit unit_coords(const KParams& p, int u) {
   return w;
 }
 
-// One pipeline stage's TMA copies into a_dst / b_dst: kAtoms swizzle atoms of A
+// One pipeline stage's TMA copies into a_dst / b_dst: ATOMS swizzle atoms of A
 // (kAtomABytes apart) and of B (kBAtom apart), all completing on barrier `bar`
 // of the leader CTA.  A convolution's stage kb is channel block kb % cblocks of
 // filter tap kb / cblocks, its A rows gathered by TMA im2col.
-template <Mode kMode, uint32_t kBAtom>
+template <Mode kMode, int ATOMS, uint32_t kBAtom>
 __device__ __forceinline__ void load_stage(const KParams& p, const CUtensorMap* tmA,
                                            const CUtensorMap* mapB, uint8_t* a_dst, uint8_t* b_dst,
                                            uint32_t bar, int kb, int m_cta, int n_cta, int cn,
                                            int ch, int cw) {
+  constexpr int kKS = BK * ATOMS;
   if constexpr (mode_is_conv(kMode)) {
     const int tap = kb / p.conv_cblocks;
-    const int c0 = (kb - tap * p.conv_cblocks) * KS;
+    const int c0 = (kb - tap * p.conv_cblocks) * kKS;
     const int r = tap / p.conv_S;
     const int s = tap - r * p.conv_S;
 #pragma unroll
-    for (int j = 0; j < kAtoms; ++j) {
+    for (int j = 0; j < ATOMS; ++j) {
       tma_load_im2col_4d_2cta(a_dst + j * kAtomABytes, tmA, bar, c0 + j * BK, cw, ch, cn,
                               static_cast<uint16_t>(s), static_cast<uint16_t>(r));
       tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, tap * p.conv_C + c0 + j * BK, n_cta);
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < kAtoms; ++j) {
-      tma_load_2d_2cta(a_dst + j * kAtomABytes, tmA, bar, kb * KS + j * BK, m_cta);
-      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, kb * KS + j * BK, n_cta);
+    for (int j = 0; j < ATOMS; ++j) {
+      tma_load_2d_2cta(a_dst + j * kAtomABytes, tmA, bar, kb * kKS + j * BK, m_cta);
+      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, kb * kKS + j * BK, n_cta);
     }
   }
 }
 
-// One pipeline stage's MMAs (kAtoms atoms x BK/16 steps of k = 16) into the
+// One pipeline stage's MMAs (ATOMS atoms x BK/16 steps of k = 16) into the
 // accumulator at d_tmem; a_st / b_st are the stage's first descriptors, B atoms
 // lie kBAtom apart.  The first MMA of a chunk overwrites the accumulator.
-template <uint32_t kBAtom>
+template <int ATOMS, uint32_t kBAtom>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint64_t a_st, uint64_t b_st,
                                           uint32_t idesc, bool accumulate) {
 #pragma unroll
-  for (int j = 0; j < kAtoms; ++j) {
+  for (int j = 0; j < ATOMS; ++j) {
 #pragma unroll
     for (int k = 0; k < BK / 16; ++k) {
       const uint64_t ad = a_st + ((j * kAtomABytes + k * 32) >> 4);
@@ -777,7 +784,7 @@ __device__ __forceinline__ void epi_float_cols(const KParams& p, const CUtensorM
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <Mode kMode, int BN>
+template <Mode kMode, int BN, int ATOMS>
 __global__ void __launch_bounds__(kThreads, 1)
     igc_tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -785,8 +792,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmO0,
                        const __grid_constant__ CUtensorMap tmO1,
                        const __grid_constant__ CUtensorMap tmO2, const KParams p) {
-  using Cfg = TileCfg<BN>;
+  using Cfg = TileCfg<BN, ATOMS>;
+  // convolutions (channel blocks) and the integer modes (exact 1024-k chunks) use the
+  // default stage depth, which the host's k-block counts assume
+  static_assert(ATOMS == kAtoms || (!mode_is_conv(kMode) && !mode_is_int(kMode)), "ATOMS");
   constexpr int kStages = Cfg::kStages;
+  constexpr uint32_t kStageABytes = Cfg::kStageABytes;
   constexpr int NC = Cfg::kEpiCols;
 
   extern __shared__ uint8_t smem_raw[];
@@ -901,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             goto producer_done;
           if (lane == 0) {
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
-            load_stage<kMode, Cfg::kAtomBBytes>(p, &tmA, mapB, sA + stage * kStageABytes,
+            load_stage<kMode, ATOMS, Cfg::kAtomBBytes>(p, &tmA, mapB, sA + stage * kStageABytes,
                                                 sB + stage * Cfg::kStageBBytes,
                                                 full_lead + static_cast<uint32_t>(stage) * 8u, kb,
                                                 m_cta, n_cta, cn, ch, cw);
@@ -939,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t a_off, b_off;
             tail_slot(stage, sw_stage, a_off, b_off);
             if (rank == 0) mbar_arrive_expect_tx(&full_t[stage], stage_tx);
-            load_stage<kMode, Cfg::kAtomBBytes / 2>(p, &tmA, mapB, smem + a_off, smem + b_off,
+            load_stage<kMode, ATOMS, Cfg::kAtomBBytes / 2>(p, &tmA, mapB, smem + a_off, smem + b_off,
                                                     full_t_lead + static_cast<uint32_t>(stage) * 8u,
                                                     kb, m_cta, n_cta, cn, ch, cw);
           }
@@ -1004,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const bool chunk_end = (kin == p.chunk_kb - 1) || (kb == p.num_kb - 1);
             if (lane == 0) {
-              mma_stage<Cfg::kAtomBBytes>(
+              mma_stage<ATOMS, Cfg::kAtomBBytes>(
                   tmem_base + static_cast<uint32_t>(acc) * Cfg::kAccStride,
                   adesc0 + ((static_cast<uint32_t>(stage) * kStageABytes) >> 4),
                   bdesc0 + ((static_cast<uint32_t>(stage) * Cfg::kStageBBytes) >> 4), idesc,
@@ -1045,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the rings share their base, sA, whose descriptor is adesc0
               uint32_t a_off, b_off;
               tail_slot(stage, sw_stage, a_off, b_off);
-              mma_stage<Cfg::kAtomBBytes / 2>(
+              mma_stage<ATOMS, Cfg::kAtomBBytes / 2>(
                   tmem_base + static_cast<uint32_t>(acc) * Cfg::kAccStride, adesc0 + (a_off >> 4),
                   adesc0 + (b_off >> 4), idesc, kin > 0);
               umma_commit_2cta_multicast(&empty_t[stage], 0x3);

@@ -27,6 +27,7 @@ unsigned long long* status_word();
 // Wait limit for kernels launched now.
 unsigned long long wait_limit_ns();
 int tile_width_override();  // 0, or the tile width set by igc_set_tile_width
+int stage_depth_override();  // 0, or the stage depth set by igc_set_stage_depth
 
 // cuTensorMapEncodeTiled / cuTensorMapEncodeIm2col through the runtime's
 // driver entry point (the library does not link libcuda directly).

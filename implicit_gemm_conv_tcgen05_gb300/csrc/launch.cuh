@@ -14,35 +14,36 @@ inline bool vec_store_ok(const void* p, long long ld, size_t esize) {
   return p == nullptr || (aligned16(p) && (static_cast<unsigned long long>(ld) * esize) % 16 == 0);
 }
 
-template <Mode kMode, int BN>
+template <Mode kMode, int BN, int ATOMS>
 struct KernelSlot {
   std::once_flag once[64];
   int rc[64];
   int max_clusters[64];
 };
 
-template <Mode kMode, int BN>
-KernelSlot<kMode, BN>& kernel_slot() {
-  static KernelSlot<kMode, BN> s;
+template <Mode kMode, int BN, int ATOMS>
+KernelSlot<kMode, BN, ATOMS>& kernel_slot() {
+  static KernelSlot<kMode, BN, ATOMS> s;
   return s;
 }
 
 // Sets the kernel's shared-memory attribute and finds how many CTA pairs fit
 // on the device at once (cached per device).
-template <Mode kMode, int BN>
+template <Mode kMode, int BN, int ATOMS = kAtoms>
 int kernel_setup(const DeviceInfo& dev, int* max_clusters) {
-  auto& s = kernel_slot<kMode, BN>();
+  using Cfg = TileCfg<BN, ATOMS>;
+  auto& s = kernel_slot<kMode, BN, ATOMS>();
   const int d = dev.device;
   std::call_once(s.once[d], [&] {
     s.rc[d] = IGC_ERR_CUDA;
     s.max_clusters[d] = 0;
-    if (dev.smem_optin < TileCfg<BN>::kSmemBytes) {
+    if (dev.smem_optin < Cfg::kSmemBytes) {
       s.rc[d] = IGC_ERR_UNSUPPORTED;
       return;
     }
-    auto kern = igc_tc_gemm_kernel<kMode, BN>;
+    auto kern = igc_tc_gemm_kernel<kMode, BN, ATOMS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(TileCfg<BN>::kSmemBytes)) != cudaSuccess)
+                             static_cast<int>(Cfg::kSmemBytes)) != cudaSuccess)
       return;
     // the kernel's register split assumes at least kMinLaunchRegs per thread at launch
     cudaFuncAttributes fa;
@@ -54,7 +55,7 @@ int kernel_setup(const DeviceInfo& dev, int* max_clusters) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -94,11 +95,11 @@ inline void add_out_map(OutMaps& o, int slot, CUtensorMapDataType dtype, const v
     o.mask |= 1 << slot;
 }
 
-template <Mode kMode, int BN>
+template <Mode kMode, int BN, int ATOMS = kAtoms>
 int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                    const CUtensorMap& tmBh, const OutMaps& om, KParams p, cudaStream_t stream) {
   int max_clusters = 0;
-  int rc = kernel_setup<kMode, BN>(dev, &max_clusters);
+  int rc = kernel_setup<kMode, BN, ATOMS>(dev, &max_clusters);
   if (rc != IGC_OK) return rc;
   p.tiles_m = static_cast<int>((static_cast<long long>(p.M) + BM - 1) / BM);
   p.tiles_n = static_cast<int>((static_cast<long long>(p.N) + BN - 1) / BN);
@@ -119,7 +120,7 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+  cfg.dynamicSmemBytes = TileCfg<BN, ATOMS>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -130,7 +131,7 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN>, tmA, tmB, tmBh, om.map[0],
+  if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN, ATOMS>, tmA, tmB, tmBh, om.map[0],
                          om.map[1], om.map[2], p) != cudaSuccess) {
     (void)cudaGetLastError();
     return IGC_ERR_CUDA;
@@ -171,6 +172,8 @@ constexpr int kBnCands[] = {256, 224, 128};
 constexpr double kBnEff[] = {1.0, 0.97, 0.87};
 constexpr int kBnCandsInt[] = {256, 128};
 constexpr double kBnEffInt[] = {1.0, 0.87};
+// shortest k for which a floating-point GEMM of at most two rounds takes 64-deep stages
+constexpr int kDeepMinK = 2048;
 
 // Picks the tile width for this problem, encodes B's tensor maps with boxes of
 // BN/2 rows (each CTA of the pair loads half of the B tile) and BN/4 rows (half
@@ -189,6 +192,24 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
                               : pick_bn(p.M, p.N, clusters, kBnCands, kBnEff, 3);
   const int forced = tile_width_override();
   if (forced == 256 || forced == 128 || (forced == 224 && !mode_is_int(kMode))) bn = forced;
+  // 64-deep stages for the floating-point GEMMs whose schedule is at most two
+  // rounds, but at least a quarter of the CTA pairs, over a long k: each unit then
+  // streams its operands mostly from DRAM (measured on GB300: +4 to +8 % at
+  // 512-1024 x 8192 x 8192, 2048 x 2048 x 8192 and 1024 x 4096 x 16384; -2 to -4 %
+  // at 2048 x 8192 x 8192 and 4096^3; -12 % at 512 x 512 x 2048, four tiles)
+  bool deep = false;
+  if constexpr (kMode == Mode::GemmF16 || kMode == Mode::GemmBF16) {
+    const long long tiles = ((static_cast<long long>(p.M) + BM - 1) / BM) *
+                            ((static_cast<long long>(p.N) + bn - 1) / bn);
+    deep = tiles <= 2LL * clusters && 4 * tiles >= clusters && p.K >= kDeepMinK;
+    const int fd = stage_depth_override();
+    if (fd == 64) deep = true;
+    if (fd == 128) deep = false;
+    if (deep) {
+      p.num_kb = (p.K + BK - 1) / BK;
+      p.chunk_kb = p.num_kb;
+    }
+  }
   CUtensorMap tmB, tmBh;  // boxes of BN/2 rows (whole tiles) and BN/4 rows (column halves)
   rc = encode_tiled_2d(&tmB, kBType, b_base, b_inner, b_rows,
                        b_row_bytes, BK, static_cast<uint32_t>(bn / 2));
@@ -196,6 +217,16 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
   rc = encode_tiled_2d(&tmBh, kBType, b_base, b_inner, b_rows,
                        b_row_bytes, BK, static_cast<uint32_t>(bn / 4));
   if (rc != IGC_OK) return rc;
+  if constexpr (kMode == Mode::GemmF16 || kMode == Mode::GemmBF16) {
+    if (deep) {
+      switch (bn) {
+        case 256: return launch_tc_gemm<kMode, 256, 1>(dev, tmA, tmB, tmBh, om, p, stream);
+        case 224: return launch_tc_gemm<kMode, 224, 1>(dev, tmA, tmB, tmBh, om, p, stream);
+        case 128: return launch_tc_gemm<kMode, 128, 1>(dev, tmA, tmB, tmBh, om, p, stream);
+        default: return IGC_ERR_UNSUPPORTED;
+      }
+    }
+  }
   if constexpr (!mode_is_int(kMode))
     if (bn == 224) return launch_tc_gemm<kMode, 224>(dev, tmA, tmB, tmBh, om, p, stream);
   switch (bn) {

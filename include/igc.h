@@ -352,6 +352,18 @@ uint64_t igc_set_wait_limit_ns(uint64_t limit_ns);
 int igc_set_tile_width(int bn);
 
 /*
+ * Tuning and test hook: the k depth of the shared-memory pipeline stages of
+ * the fp16 / bf16 GEMMs launched after this call.  0 (the default) picks it
+ * per problem: 64-deep stages (twice as many, more bytes in flight) when the
+ * schedule is at most two rounds of tiles over the CTA pairs, the tiles fill
+ * at least a quarter of them and K >= 2048, else 128-deep; 64 or 128 force it.  Convolutions and the integer paths
+ * always use 128.  Results do not depend on the depth beyond fp32 rounding
+ * order.  Returns the previous setting, or -1 (and changes nothing) for any
+ * other value.  Process-wide.
+ */
+int igc_set_stage_depth(int k);
+
+/*
  * Diagnostic: launches one CTA that waits on an mbarrier nothing ever
  * completes, with the current wait limit, and returns.  The wait gives up
  * after the limit and records IGC_ERR_DEVICE_TIMEOUT for

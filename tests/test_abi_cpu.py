@@ -17,7 +17,8 @@ def test_library_loads_and_exports_every_declared_symbol():
                 "gemm_s8_zp_run", "gemm_s8_zp_dequant", "gemm_s8_zp_noalloc",
                 "conv2d_nhwc_s8_zp", "conv2d_nhwc_s8_zp_workspace_size", "conv2d_nhwc_f16_implicit",
                 "igc_status_string", "igc_check_device_status", "igc_last_device_status",
-                "igc_set_wait_limit_ns", "igc_set_tile_width", "igc_debug_wait_timeout_probe",
+                "igc_set_wait_limit_ns", "igc_set_tile_width", "igc_set_stage_depth",
+                "igc_debug_wait_timeout_probe",
                 "igc_version"}
     assert expected <= set(names)
     for n in names:
@@ -105,3 +106,10 @@ def test_tile_width_setter_roundtrip():
     assert igc.igc_set_tile_width(96) == -1          # not a built width: unchanged
     assert igc.igc_set_tile_width(128) == 224
     assert igc.igc_set_tile_width(0) == 128
+
+
+def test_stage_depth_setter_roundtrip():
+    assert igc.igc_set_stage_depth(64) == 0
+    assert igc.igc_set_stage_depth(96) == -1         # not a built depth: unchanged
+    assert igc.igc_set_stage_depth(128) == 64
+    assert igc.igc_set_stage_depth(0) == 128
