@@ -340,6 +340,18 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
     ms = t_ms(lambda: torch.matmul(A, B.t(), out=C))
     out["context_torch_matmul_f16_4096^3"] = {"ms": ms, "tflops": 2 * 4096 ** 3 / ms / 1e9}
     del A, B, C
+    # the vendor library's fp16 convolution (cuDNN through torch, algorithm autotuned)
+    # on the step's convolution inputs, NHWC memory (context only)
+    w4 = synth.workload(4)
+    xc = t(w4["x"]).permute(0, 3, 1, 2)  # NCHW view of the NHWC tensor (channels_last)
+    wc = t(w4["w"]).permute(0, 3, 1, 2)  # K x C x R x S view of the KRSC tensor
+    prev_bench = torch.backends.cudnn.benchmark
+    torch.backends.cudnn.benchmark = True
+    ms = t_ms(lambda: torch.nn.functional.conv2d(xc, wc, padding=1))
+    torch.backends.cudnn.benchmark = prev_bench
+    out["context_cudnn_conv3x3_256x14x14x256->512"] = {
+        "ms": ms, "tflops": OPS["conv3x3_256x14x14x256_512"] / ms / 1e9}
+    del xc, wc, w4
     # int8 GEMM 8192^3 with the dequantised fp32 output (dequantise + bias fused)
     w5 = synth.workload(5)
     Aq, Bq = t(w5["A"]), t(w5["Bt"])

@@ -263,32 +263,51 @@ __device__ __forceinline__ Unit unit_coords(const KParams& p, int u) {
   return w;
 }
 
+// Where a pipeline stage lies along k: for a GEMM, k0 is the k of its first
+// atom in A and B; for a convolution, k0 is the channel offset within filter
+// tap (r, s) and bcol the matching column of the K x (R*S*C) weights.  The
+// producer advances it stage by stage (advance), with no division in its loop.
+struct StagePos {
+  int k0, r, s, bcol;
+};
+
+template <Mode kMode, int ATOMS>
+__device__ __forceinline__ void advance(StagePos& q, const KParams& p, int tap_end) {
+  constexpr int kKS = BK * ATOMS;
+  q.k0 += kKS;
+  q.bcol += kKS;
+  if constexpr (mode_is_conv(kMode)) {
+    if (q.k0 == tap_end) {  // next filter tap: channel block 0, columns from tap * C
+      q.k0 = 0;
+      q.bcol += p.conv_C - tap_end;
+      if (++q.s == p.conv_S) {
+        q.s = 0;
+        ++q.r;
+      }
+    }
+  }
+}
+
 // One pipeline stage's TMA copies into a_dst / b_dst: ATOMS swizzle atoms of A
 // (kAtomABytes apart) and of B (kBAtom apart), all completing on barrier `bar`
-// of the leader CTA.  A convolution's stage kb is channel block kb % cblocks of
-// filter tap kb / cblocks, its A rows gathered by TMA im2col.
+// of the leader CTA.  A convolution's A rows are gathered by TMA im2col.
 template <Mode kMode, int ATOMS, uint32_t kBAtom>
-__device__ __forceinline__ void load_stage(const KParams& p, const CUtensorMap* tmA,
-                                           const CUtensorMap* mapB, uint8_t* a_dst, uint8_t* b_dst,
-                                           uint32_t bar, int kb, int m_cta, int n_cta, int cn,
-                                           int ch, int cw) {
-  constexpr int kKS = BK * ATOMS;
+__device__ __forceinline__ void load_stage(const CUtensorMap* tmA, const CUtensorMap* mapB,
+                                           uint8_t* a_dst, uint8_t* b_dst, uint32_t bar,
+                                           const StagePos& q, int m_cta, int n_cta, int cn, int ch,
+                                           int cw) {
   if constexpr (mode_is_conv(kMode)) {
-    const int tap = kb / p.conv_cblocks;
-    const int c0 = (kb - tap * p.conv_cblocks) * kKS;
-    const int r = tap / p.conv_S;
-    const int s = tap - r * p.conv_S;
 #pragma unroll
     for (int j = 0; j < ATOMS; ++j) {
-      tma_load_im2col_4d_2cta(a_dst + j * kAtomABytes, tmA, bar, c0 + j * BK, cw, ch, cn,
-                              static_cast<uint16_t>(s), static_cast<uint16_t>(r));
-      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, tap * p.conv_C + c0 + j * BK, n_cta);
+      tma_load_im2col_4d_2cta(a_dst + j * kAtomABytes, tmA, bar, q.k0 + j * BK, cw, ch, cn,
+                              static_cast<uint16_t>(q.s), static_cast<uint16_t>(q.r));
+      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, q.bcol + j * BK, n_cta);
     }
   } else {
 #pragma unroll
     for (int j = 0; j < ATOMS; ++j) {
-      tma_load_2d_2cta(a_dst + j * kAtomABytes, tmA, bar, kb * kKS + j * BK, m_cta);
-      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, kb * kKS + j * BK, n_cta);
+      tma_load_2d_2cta(a_dst + j * kAtomABytes, tmA, bar, q.k0 + j * BK, m_cta);
+      tma_load_2d_2cta(b_dst + j * kBAtom, mapB, bar, q.bcol + j * BK, n_cta);
     }
   }
 }
@@ -793,9 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmO1,
                        const __grid_constant__ CUtensorMap tmO2, const KParams p) {
   using Cfg = TileCfg<BN, ATOMS>;
-  // convolutions (channel blocks) and the integer modes (exact 1024-k chunks) use the
-  // default stage depth, which the host's k-block counts assume
-  static_assert(ATOMS == kAtoms || (!mode_is_conv(kMode) && !mode_is_int(kMode)), "ATOMS");
+  // the integer modes (exact 1024-k chunks of kIntChunkKb stages) use the default depth
+  static_assert(ATOMS == kAtoms || !mode_is_int(kMode), "ATOMS");
   constexpr int kStages = Cfg::kStages;
   constexpr uint32_t kStageABytes = Cfg::kStageABytes;
   constexpr int NC = Cfg::kEpiCols;
@@ -884,6 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int sw_stage = -1;
     uint32_t sw_phase = 0;
     long long issued_main = 0;
+    // a convolution's stages walk the channel blocks of each filter tap in turn
+    const int tap_end = p.conv_cblocks * Cfg::kKS;
     for (int u = cluster; u < p.num_units; u += num_clusters) {
       const Unit w = unit_coords(p, u);
       const int mb = w.mb;
@@ -905,6 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ch = pp * p.stride_h - p.pad_h;
         cw = qq * p.stride_w - p.pad_w;
       }
+      StagePos q{0, 0, 0, 0};
       if (!Cfg::kTailRing || !w.half) {
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, lim, abort_flag,
@@ -912,12 +933,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             goto producer_done;
           if (lane == 0) {
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
-            load_stage<kMode, ATOMS, Cfg::kAtomBBytes>(p, &tmA, mapB, sA + stage * kStageABytes,
-                                                sB + stage * Cfg::kStageBBytes,
-                                                full_lead + static_cast<uint32_t>(stage) * 8u, kb,
-                                                m_cta, n_cta, cn, ch, cw);
+            load_stage<kMode, ATOMS, Cfg::kAtomBBytes>(
+                &tmA, mapB, sA + stage * kStageABytes, sB + stage * Cfg::kStageBBytes,
+                full_lead + static_cast<uint32_t>(stage) * 8u, q, m_cta, n_cta, cn, ch, cw);
           }
           __syncwarp();
+          advance<kMode, ATOMS>(q, p, tap_end);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -950,11 +971,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t a_off, b_off;
             tail_slot(stage, sw_stage, a_off, b_off);
             if (rank == 0) mbar_arrive_expect_tx(&full_t[stage], stage_tx);
-            load_stage<kMode, ATOMS, Cfg::kAtomBBytes / 2>(p, &tmA, mapB, smem + a_off, smem + b_off,
-                                                    full_t_lead + static_cast<uint32_t>(stage) * 8u,
-                                                    kb, m_cta, n_cta, cn, ch, cw);
+            load_stage<kMode, ATOMS, Cfg::kAtomBBytes / 2>(
+                &tmA, mapB, smem + a_off, smem + b_off,
+                full_t_lead + static_cast<uint32_t>(stage) * 8u, q, m_cta, n_cta, cn, ch, cw);
           }
           __syncwarp();
+          advance<kMode, ATOMS>(q, p, tap_end);
           ++issued;
           if (++stage == Cfg::kTailStages) {
             stage = 0;

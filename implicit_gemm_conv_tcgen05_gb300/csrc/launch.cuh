@@ -198,15 +198,22 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
   // 512-1024 x 8192 x 8192, 2048 x 2048 x 8192 and 1024 x 4096 x 16384; -2 to -4 %
   // at 2048 x 8192 x 8192 and 4096^3; -12 % at 512 x 512 x 2048, four tiles)
   bool deep = false;
-  if constexpr (kMode == Mode::GemmF16 || kMode == Mode::GemmBF16) {
+  if constexpr (!mode_is_int(kMode)) {
     const long long tiles = ((static_cast<long long>(p.M) + BM - 1) / BM) *
                             ((static_cast<long long>(p.N) + bn - 1) / bn);
-    deep = tiles <= 2LL * clusters && 4 * tiles >= clusters && p.K >= kDeepMinK;
+    if constexpr (!mode_is_conv(kMode))
+      deep = tiles <= 2LL * clusters && 4 * tiles >= clusters && p.K >= kDeepMinK;
     const int fd = stage_depth_override();
     if (fd == 64) deep = true;
     if (fd == 128) deep = false;
     if (deep) {
-      p.num_kb = (p.K + BK - 1) / BK;
+      if constexpr (mode_is_conv(kMode)) {  // channel blocks of BK per filter tap
+        const int taps = p.num_kb / p.conv_cblocks;
+        p.conv_cblocks = (p.conv_C + BK - 1) / BK;
+        p.num_kb = taps * p.conv_cblocks;
+      } else {
+        p.num_kb = (p.K + BK - 1) / BK;
+      }
       p.chunk_kb = p.num_kb;
     }
   }
@@ -217,7 +224,7 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
   rc = encode_tiled_2d(&tmBh, kBType, b_base, b_inner, b_rows,
                        b_row_bytes, BK, static_cast<uint32_t>(bn / 4));
   if (rc != IGC_OK) return rc;
-  if constexpr (kMode == Mode::GemmF16 || kMode == Mode::GemmBF16) {
+  if constexpr (!mode_is_int(kMode)) {
     if (deep) {
       switch (bn) {
         case 256: return launch_tc_gemm<kMode, 256, 1>(dev, tmA, tmB, tmBh, om, p, stream);

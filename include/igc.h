@@ -353,13 +353,14 @@ int igc_set_tile_width(int bn);
 
 /*
  * Tuning and test hook: the k depth of the shared-memory pipeline stages of
- * the fp16 / bf16 GEMMs launched after this call.  0 (the default) picks it
- * per problem: 64-deep stages (twice as many, more bytes in flight) when the
- * schedule is at most two rounds of tiles over the CTA pairs, the tiles fill
- * at least a quarter of them and K >= 2048, else 128-deep; 64 or 128 force it.  Convolutions and the integer paths
- * always use 128.  Results do not depend on the depth beyond fp32 rounding
- * order.  Returns the previous setting, or -1 (and changes nothing) for any
- * other value.  Process-wide.
+ * the fp16 / bf16 GEMMs and the fp16 convolution launched after this call.
+ * 0 (the default) picks it per problem: 64-deep stages (twice as many, more
+ * bytes in flight) for a GEMM whose schedule is at most two rounds of tiles
+ * over the CTA pairs, whose tiles fill at least a quarter of them and whose
+ * K >= 2048, else 128-deep (always 128 for a convolution); 64 or 128 force
+ * it.  The integer paths always use 128.  Results do not depend on the depth
+ * beyond fp32 rounding order.  Returns the previous setting, or -1 (and
+ * changes nothing) for any other value.  Process-wide.
  */
 int igc_set_stage_depth(int k);
 

@@ -75,3 +75,23 @@ def test_gemm_f16_automatic_deep_stages(M, N, K):
     check_device_ok()
     ref, _ = oracle.gemm_f16(A, Bt)
     assert np.array_equal(host(C32), ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("N,H,W,C,K,R,S,pad,stride", [
+    (3, 10, 11, 64, 200, 3, 3, (1, 1), (1, 1)),
+    (2, 9, 9, 72, 96, 3, 3, (1, 1), (1, 1)),     # C not a multiple of 64: zero-filled channels
+    (2, 12, 13, 136, 64, 5, 3, (2, 1), (2, 1)),
+    (4, 14, 14, 256, 512, 3, 3, (1, 1), (1, 1)),
+])
+def test_conv_f16_every_depth(depth, N, H, W, C, K, R, S, pad, stride):
+    x = synth.normal_f16(N * 31 + C, 6, (N, H, W, C))
+    w = synth.normal_f16(K * 31 + R, 7, (K, R, S, C), std=1.0 / np.sqrt(R * S * C))
+    P = (H + 2 * pad[0] - R) // stride[0] + 1
+    Q = (W + 2 * pad[1] - S) // stride[1] + 1
+    y = torch.empty((N, P, Q, K), dtype=torch.float16, device="cuda")
+    y32 = torch.empty((N, P, Q, K), dtype=torch.float32, device="cuda")
+    igc.conv2d_nhwc_f16_implicit(dev(x), dev(w), y, y32, pad=pad, stride=stride)
+    check_device_ok()
+    ref, sabs = oracle.conv2d_nhwc_f16(x, w, pad=pad, stride=stride)
+    assert_fp16_bound(host(y32), ref, sabs, f"conv depth {depth}")
+    assert_f16_is_rne_of_f32(host(y), host(y32), f"conv depth {depth}")
