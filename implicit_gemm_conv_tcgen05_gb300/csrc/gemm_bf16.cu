@@ -42,6 +42,8 @@ extern "C" int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t
   p.K = static_cast<int>(K);
   p.num_kb = static_cast<int>((K + KS - 1) / KS);
   p.chunk_kb = p.num_kb;
+  p.pf_a = static_cast<const char*>(A);
+  p.pf_lda = lda * 2;
   p.out = C;
   p.ldo = ldc;
   p.out_type = c_dtype == IGC_BF16 ? kOutBF16 : kOutF32;

@@ -155,6 +155,8 @@ int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, in
   p.K = static_cast<int>(K);
   p.num_kb = static_cast<int>((Kp + KS - 1) / KS);
   p.chunk_kb = kIntChunkKb;
+  p.pf_a = reinterpret_cast<const char*>(ws + l.a_off);
+  p.pf_lda = Kp * 2;
   p.c32 = C32;
   p.ldc32 = ldc32;
   p.c8 = C8;

@@ -227,6 +227,13 @@ struct KParams {
   const float* bias;
   unsigned long long wait_limit_ns;
   unsigned long long* status;
+  // GEMMs: the operands' rows (row strides in bytes, k extent in bytes) for the L2
+  // prefetch of the first pf_units work units of each CTA pair (0: none)
+  const char* pf_a;
+  const char* pf_b;
+  long long pf_lda, pf_ldb;
+  int pf_kbytes;
+  int pf_units;
 };
 
 __device__ __forceinline__ void tile_coords(const KParams& p, int t, int& mb, int& nb) {
@@ -261,6 +268,67 @@ __device__ __forceinline__ Unit unit_coords(const KParams& p, int u) {
   }
   tile_coords(p, t, w.mb, w.nb);
   return w;
+}
+
+// L2 prefetch of k bytes [k0, k0 + kb) of `nrows` operand rows from row0 (rows
+// past rows_total and bytes past kbytes skipped), by the 64 threads t = 0..63
+// of warps 2-3, one 128-byte line each.
+__device__ __forceinline__ void prefetch_rows(const char* base, long long ld, int row0, int nrows,
+                                              int rows_total, int k0, int kb, int kbytes, int t) {
+  const int lines = kb / 128;
+  for (int i = t; i < nrows * lines; i += 64) {
+    const int r = i / lines;
+    const int kc = k0 + (i - r * lines) * 128;
+    const int row = row0 + r;
+    if (row < rows_total && kc < kbytes)
+      prefetch_l2(base + static_cast<long long>(row) * ld + kc);
+  }
+}
+
+// Warps 2-3 of a GEMM: L2 prefetch of the A and B rows of this CTA's first
+// p.pf_units work units (whole tiles), kPrefetchAhead stages ahead of the
+// producer's copies, which it publishes in *progress (stages issued).  The first
+// rounds of a schedule take all their panels from DRAM in lockstep, and three
+// ring stages do not cover DRAM latency; lines requested this far ahead are in
+// L2 when the copies ask for them.  A panel is prefetched only by the unit that
+// first uses it in its round (the one with the same m-tile one group column back,
+// or the previous tile with the same n-tile, is in the round already otherwise),
+// so each line is requested about once.  The waits are bounded and give up
+// silently: a prefetch is only a hint.
+template <int BN, int kStageKBytes>
+__device__ __forceinline__ void prefetch_first_units(const KParams& p, int cluster, int num_clusters,
+                                                     uint32_t rank, int t,
+                                                     const volatile int* progress,
+                                                     const volatile int* abort) {
+  constexpr int kPrefetchAhead = 6;
+  const uint64_t t0 = globaltimer_ns();
+  for (int i = 0; i < p.pf_units; ++i) {
+    const int u = cluster + i * num_clusters;
+    if (u >= p.tail_start) return;  // whole tiles only
+    int mb, nb;
+    tile_coords(p, u, mb, nb);
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = u / per_group;
+    const int gstart = g * per_group;
+    const int gm = min(p.tiles_m - g * p.group_m, p.group_m);
+    const int lo = max(u - cluster, gstart);  // first unit of this round within the group
+    const bool first_a = u - gm < lo;
+    const bool first_b = u - 1 < max(lo, gstart + nb * gm);
+    if (!first_a && !first_b) continue;
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      const int need = i * p.num_kb + kb - kPrefetchAhead;  // producer stages issued first
+      while (*progress < need) {
+        if (*abort || globaltimer_ns() - t0 > 20000000ull) return;
+        __nanosleep(200);
+      }
+      if (first_a)
+        prefetch_rows(p.pf_a, p.pf_lda, mb * BM + static_cast<int>(rank) * BM_CTA, BM_CTA, p.M,
+                      kb * kStageKBytes, kStageKBytes, p.pf_kbytes, t);
+      if (first_b)
+        prefetch_rows(p.pf_b, p.pf_ldb, nb * BN + static_cast<int>(rank) * (BN / 2), BN / 2, p.N,
+                      kb * kStageKBytes, kStageKBytes, p.pf_kbytes, t);
+    }
+  }
 }
 
 // Where a pipeline stage lies along k: for a GEMM, k0 is the k of its first
@@ -835,6 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty_t = full_t + Cfg::kTailStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_t + Cfg::kTailStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* progress = abort_flag + 1;  // producer: stages issued (read by the prefetch)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
   const int lane = static_cast<int>(lane_id());
@@ -859,6 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     *abort_flag = 0;
+    *progress = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -940,6 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           advance<kMode, ATOMS>(q, p, tap_end);
           ++issued;
+          if (lane == 0) *progress = static_cast<int>(issued);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -1106,6 +1177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+    } else if (pair_ok && p.pf_units > 0) {
+    // ------------------------------------------------------------ L2 prefetch (warps 2-3)
+      if constexpr (!mode_is_conv(kMode))
+        prefetch_first_units<BN, Cfg::kKS * 2>(p, cluster, num_clusters, rank,
+                                               (warp - 2) * 32 + lane, progress, abort_flag);
     }
   } else {
     warpgroup_regs_inc<kRegsHigh>();

@@ -174,6 +174,9 @@ constexpr int kBnCandsInt[] = {256, 128};
 constexpr double kBnEffInt[] = {1.0, 0.87};
 // shortest k for which a floating-point GEMM of at most two rounds takes 64-deep stages
 constexpr int kDeepMinK = 2048;
+// GEMMs whose operands take at most this many bytes (half of the 129 MB L2) prefetch
+// the panels of each CTA pair's first two work units, larger ones of the first only
+constexpr double kPrefetchTwoUnitsBytes = 64.0 * 1024 * 1024;
 
 // Picks the tile width for this problem, encodes B's tensor maps with boxes of
 // BN/2 rows (each CTA of the pair loads half of the B tile) and BN/4 rows (half
@@ -215,6 +218,17 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
         p.num_kb = (p.K + BK - 1) / BK;
       }
       p.chunk_kb = p.num_kb;
+    }
+  }
+  if constexpr (!mode_is_conv(kMode)) {
+    // L2 prefetch of the first rounds' panels (the entry set pf_a / pf_lda)
+    if (p.pf_a != nullptr && p.K <= (1 << 29)) {
+      p.pf_b = static_cast<const char*>(b_base);
+      p.pf_ldb = static_cast<long long>(b_row_bytes);
+      p.pf_kbytes = p.K * 2;
+      const double bytes = static_cast<double>(p.M) * static_cast<double>(p.pf_lda) +
+                           static_cast<double>(p.N) * static_cast<double>(p.pf_ldb);
+      p.pf_units = bytes <= kPrefetchTwoUnitsBytes ? 2 : 1;
     }
   }
   CUtensorMap tmB, tmBh;  // boxes of BN/2 rows (whole tiles) and BN/4 rows (column halves)

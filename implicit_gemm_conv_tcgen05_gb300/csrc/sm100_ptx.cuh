@@ -125,6 +125,11 @@ __device__ __forceinline__ void grid_dependents_launch() {
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), completion signalled on an mbarrier
 // ---------------------------------------------------------------------------
+// Brings the 128-byte line holding global address `a` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(a)));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
