@@ -656,6 +656,61 @@ def run_reference(args):
     }
 
 
+def profile_case(name: str) -> int:
+    """Untimed calls for ncu captures of rows outside the step (no JSON line).
+
+    small: the two small configurations, each called four times (fp16 256^3 with
+    fp32 out; int8 1024^3 with C32 + C8).  weak: three weaker extras rows called
+    twice each after an L2 flush, in order stride-2 fp16 conv, fp16 512 x 8192 x
+    8192, int8 conv.  Prints the device status word's verdict."""
+    import torch
+    import implicit_gemm_conv_tcgen05_gb300 as igc
+    torch.cuda.set_device(0)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    if name == "small":
+        w1 = synth.workload(1)
+        A1, B1 = t(w1["A"]), t(w1["Bt"])
+        C1 = torch.empty((256, 256), dtype=torch.float32, device="cuda")
+        w2 = synth.workload(2)
+        A2, B2 = t(w2["A"]), t(w2["Bt"])
+        C32 = torch.empty((1024, 1024), dtype=torch.int32, device="cuda")
+        C8 = torch.empty((1024, 1024), dtype=torch.int8, device="cuda")
+        ws = torch.empty(igc.gemm_s8_zp_workspace_size(1024, 1024, 1024), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(4):
+            igc.gemm_f16(A1, B1, C1)
+        for _ in range(4):
+            igc.gemm_s8_zp(A2, B2, zA=128, zB=121, C32=C32, C8=C8, scale=w2["scale"],
+                           workspace=ws)
+    elif name == "weak":
+        xs = t(synth.normal_f16(44, 6, (256, 28, 28, 128)))
+        wsx = t(synth.normal_f16(44, 7, (256, 3, 3, 128), std=1 / 34.0))
+        ys = torch.empty((256, 14, 14, 256), dtype=torch.float16, device="cuda")
+        Bk = t(synth.normal_f16(45, 2, (8192, 8192)))
+        Am = t(synth.normal_f16(45 + 512, 1, (512, 8192)))
+        Cm = torch.empty((512, 8192), dtype=torch.float16, device="cuda")
+        x8 = t(synth.uniform_int(43, 6, (256, 14, 14, 256), 0, 255, np.uint8))
+        w8 = t(synth.uniform_int(43, 7, (512, 3, 3, 256), -127, 127, np.int8))
+        y8 = torch.empty((256, 14, 14, 512), dtype=torch.int8, device="cuda")
+        sk = t(synth.uniform_f32(43, 5, (512,), 1e-4, 1e-3))
+        wsc = torch.empty(igc.conv2d_nhwc_s8_zp_workspace_size(256, 14, 14, 256, 512, 3, 3),
+                          dtype=torch.uint8, device="cuda")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            flush.zero_()
+            igc.conv2d_nhwc_f16_implicit(xs, wsx, ys, pad=(1, 1), stride=(2, 2))
+            flush.zero_()
+            igc.gemm_f16(Am, Bk, Cm)
+            flush.zero_()
+            igc.conv2d_nhwc_s8_zp(x8, w8, 128, y8=y8, scale_k=sk, workspace=wsc)
+    else:
+        raise ValueError(name)
+    torch.cuda.synchronize()
+    rc = igc.igc_check_device_status()
+    print("device status", igc.status_string(rc), flush=True)
+    return 0 if rc == igc.IGC_OK else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -666,7 +721,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile-case", choices=["small", "weak"], default=None,
+                    help="run untimed calls of rows outside the step for an ncu capture")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return profile_case(args.profile_case)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
