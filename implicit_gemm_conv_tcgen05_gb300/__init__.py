@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
             L.igc_set_tile_width.restype = i32
             L.igc_set_stage_depth.argtypes = [i32]
             L.igc_set_stage_depth.restype = i32
+            L.igc_plan_gemm.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int32)]
+            L.igc_plan_gemm.restype = i32
             L.igc_debug_wait_timeout_probe.argtypes = [vp]
             L.igc_debug_wait_timeout_probe.restype = i32
             L.igc_version.argtypes = []
@@ -177,6 +179,19 @@ def igc_set_tile_width(bn: int) -> int:
 
 def igc_set_stage_depth(k: int) -> int:
     return int(lib().igc_set_stage_depth(int(k)))
+
+
+PLAN_GEMM_F16, PLAN_GEMM_BF16, PLAN_GEMM_S8 = 0, 1, 2
+_PLAN_FIELDS = ("tile_width", "stage_k", "tiles_m", "tiles_n", "tail_start", "units", "ctas",
+                "prefetch_units")
+
+
+def igc_plan_gemm(op: int, M: int, N: int, K: int, clusters: int = 0) -> dict:
+    """The schedule a GEMM call would run with (see include/igc.h); raises on error."""
+    out = (ctypes.c_int32 * 8)()
+    _check(lib().igc_plan_gemm(int(op), int(M), int(N), int(K), int(clusters), out),
+           "igc_plan_gemm")
+    return dict(zip(_PLAN_FIELDS, (int(v) for v in out)))
 
 
 def igc_set_wait_limit_ns(limit_ns: int) -> int:

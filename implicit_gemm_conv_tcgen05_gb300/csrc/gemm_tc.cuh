@@ -144,7 +144,7 @@ enum : uint32_t {
 //   slot 0: A(m0), B(m0) low half     slot 1: A(m1), B(m0) high half
 //   slot 2: B(m1), B(m2) low half     slot 3: A(m2), B(m2) high half
 // Slot i's first fill therefore needs main stages m0..m_min(i,2) released, in order.
-__device__ __forceinline__ void tail_slot(int i, int m0, uint32_t& a_off, uint32_t& b_off) {
+__host__ __device__ constexpr void tail_slot(int i, int m0, uint32_t& a_off, uint32_t& b_off) {
   constexpr uint32_t kS = 32768u, kB0 = 3u * 32768u, kHalfB = 16384u;
   const uint32_t m1 = m0 == 2 ? 0u : static_cast<uint32_t>(m0) + 1u;
   const uint32_t m2 = m1 == 2u ? 0u : m1 + 1u;
@@ -163,6 +163,44 @@ __device__ __forceinline__ void tail_slot(int i, int m0, uint32_t& a_off, uint32
     b_off = kB0 + m2 * kS + kHalfB;
   }
 }
+
+// Compile-time check of the tail-ring map for every oldest main stage m0: the four
+// slots' A (32 KB) and B (16 KB) parts are 1024-byte aligned, disjoint, cover the
+// three main stages' 192 KB exactly, and slot i overlaps only main stages released
+// no later than m_min(i,2), the ones its first fill waits for.
+constexpr bool tail_ring_map_ok() {
+  constexpr uint32_t kS = 32768u, kB0 = 3u * 32768u;
+  for (int m0 = 0; m0 < 3; ++m0) {
+    uint32_t lo[8] = {}, hi[8] = {};
+    uint32_t total = 0;
+    for (int i = 0; i < 4; ++i) {
+      uint32_t a = 0, b = 0;
+      tail_slot(i, m0, a, b);
+      lo[2 * i] = a;
+      hi[2 * i] = a + kS;
+      lo[2 * i + 1] = b;
+      hi[2 * i + 1] = b + kS / 2;
+      total += kS + kS / 2;
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t l = lo[2 * i + part], h = hi[2 * i + part];
+        if (l % 1024u != 0 || h > 6u * kS) return false;
+        // main stages this part overlaps must be among m0 .. m_min(i,2)
+        for (int ms = 0; ms < 3; ++ms) {
+          const uint32_t la = ms * kS, ha = la + kS, lb = kB0 + ms * kS, hb = lb + kS;
+          const bool overlaps = (l < ha && la < h) || (l < hb && lb < h);
+          const int order = (ms - m0 + 3) % 3;  // release order of main stage ms
+          if (overlaps && order > (i < 2 ? i : 2)) return false;
+        }
+      }
+    }
+    for (int x = 0; x < 8; ++x)
+      for (int y = x + 1; y < 8; ++y)
+        if (lo[x] < hi[y] && lo[y] < hi[x]) return false;
+    if (total != 6u * kS) return false;
+  }
+  return true;
+}
+static_assert(tail_ring_map_ok(), "tail ring map");
 
 // Leader CTA, after an abort: waits (briefly) for the last fills of a ring whose
 // next fill would be `stage` in `phase`, so that no copy is still landing when the

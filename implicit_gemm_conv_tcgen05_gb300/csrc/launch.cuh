@@ -95,6 +95,14 @@ inline void add_out_map(OutMaps& o, int slot, CUtensorMapDataType dtype, const v
     o.mask |= 1 << slot;
 }
 
+// First unit index of the column-half tail: when the last round of the schedule
+// would be at most half full, its tiles run as column halves (the round holds
+// twice the units at half the length); otherwise there is no tail.
+inline int tail_start_of(int num_tiles, int clusters) {
+  const int rem = num_tiles % clusters;
+  return (rem > 0 && 2 * rem <= clusters) ? num_tiles - rem : num_tiles;
+}
+
 template <Mode kMode, int BN, int ATOMS = kAtoms>
 int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensorMap& tmB,
                    const CUtensorMap& tmBh, const OutMaps& om, KParams p, cudaStream_t stream) {
@@ -107,10 +115,7 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   if (tiles > 0x7fff0000LL) return IGC_ERR_UNSUPPORTED;  // units (tiles + tail halves) fit an int
   p.num_tiles = static_cast<int>(tiles);
   p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;  // m-tiles walked together (measured best of 2-16)
-  // When the last round of the schedule would be at most half full, its tiles
-  // run as column halves: the round holds twice the units at half the length.
-  const int rem = p.num_tiles % max_clusters;
-  p.tail_start = (rem > 0 && 2 * rem <= max_clusters) ? p.num_tiles - rem : p.num_tiles;
+  p.tail_start = tail_start_of(p.num_tiles, max_clusters);
   p.num_units = p.num_tiles + (p.num_tiles - p.tail_start);
   p.wait_limit_ns = wait_limit_ns();
   p.status = status_word();
@@ -178,6 +183,29 @@ constexpr int kDeepMinK = 2048;
 // the panels of each CTA pair's first two work units, larger ones of the first only
 constexpr double kPrefetchTwoUnitsBytes = 64.0 * 1024 * 1024;
 
+// The automatic stage depth of a floating-point GEMM: 64-deep stages when its
+// schedule is at most two rounds, but at least a quarter of the CTA pairs, over a
+// long k: each unit then streams its operands mostly from DRAM (measured on GB300:
+// +4 to +8 % at 512-1024 x 8192 x 8192, 2048 x 2048 x 8192 and 1024 x 4096 x
+// 16384; -2 to -4 % at 2048 x 8192 x 8192 and 4096^3; -12 % at 512 x 512 x 2048,
+// four tiles).
+inline bool auto_deep_stages(long long M, long long N, long long K, int bn, int clusters) {
+  const long long tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  return tiles <= 2LL * clusters && 4 * tiles >= clusters && K >= kDeepMinK;
+}
+
+// Leading work units per CTA pair whose panels the prefetch warps bring into L2.
+inline int prefetch_units_of(double operand_bytes) {
+  return operand_bytes <= kPrefetchTwoUnitsBytes ? 2 : 1;
+}
+
+// Tile width after an igc_set_tile_width override (integer modes have no 224).
+inline int apply_width_override(int bn, bool int_mode) {
+  const int forced = tile_width_override();
+  if (forced == 256 || forced == 128 || (forced == 224 && !int_mode)) return forced;
+  return bn;
+}
+
 // Picks the tile width for this problem, encodes B's tensor maps with boxes of
 // BN/2 rows (each CTA of the pair loads half of the B tile) and BN/4 rows (half
 // of a column-half unit's B) and launches.
@@ -193,19 +221,10 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
   if (rc != IGC_OK) return rc;
   int bn = mode_is_int(kMode) ? pick_bn(p.M, p.N, clusters, kBnCandsInt, kBnEffInt, 2)
                               : pick_bn(p.M, p.N, clusters, kBnCands, kBnEff, 3);
-  const int forced = tile_width_override();
-  if (forced == 256 || forced == 128 || (forced == 224 && !mode_is_int(kMode))) bn = forced;
-  // 64-deep stages for the floating-point GEMMs whose schedule is at most two
-  // rounds, but at least a quarter of the CTA pairs, over a long k: each unit then
-  // streams its operands mostly from DRAM (measured on GB300: +4 to +8 % at
-  // 512-1024 x 8192 x 8192, 2048 x 2048 x 8192 and 1024 x 4096 x 16384; -2 to -4 %
-  // at 2048 x 8192 x 8192 and 4096^3; -12 % at 512 x 512 x 2048, four tiles)
+  bn = apply_width_override(bn, mode_is_int(kMode));
   bool deep = false;
   if constexpr (!mode_is_int(kMode)) {
-    const long long tiles = ((static_cast<long long>(p.M) + BM - 1) / BM) *
-                            ((static_cast<long long>(p.N) + bn - 1) / bn);
-    if constexpr (!mode_is_conv(kMode))
-      deep = tiles <= 2LL * clusters && 4 * tiles >= clusters && p.K >= kDeepMinK;
+    if constexpr (!mode_is_conv(kMode)) deep = auto_deep_stages(p.M, p.N, p.K, bn, clusters);
     const int fd = stage_depth_override();
     if (fd == 64) deep = true;
     if (fd == 128) deep = false;
@@ -226,9 +245,8 @@ int launch_auto_bn(const DeviceInfo& dev, const CUtensorMap& tmA, const void* b_
       p.pf_b = static_cast<const char*>(b_base);
       p.pf_ldb = static_cast<long long>(b_row_bytes);
       p.pf_kbytes = p.K * 2;
-      const double bytes = static_cast<double>(p.M) * static_cast<double>(p.pf_lda) +
-                           static_cast<double>(p.N) * static_cast<double>(p.pf_ldb);
-      p.pf_units = bytes <= kPrefetchTwoUnitsBytes ? 2 : 1;
+      p.pf_units = prefetch_units_of(static_cast<double>(p.M) * static_cast<double>(p.pf_lda) +
+                                     static_cast<double>(p.N) * static_cast<double>(p.pf_ldb));
     }
   }
   CUtensorMap tmB, tmBh;  // boxes of BN/2 rows (whole tiles) and BN/4 rows (column halves)

@@ -373,6 +373,31 @@ int igc_set_stage_depth(int k);
  */
 int igc_debug_wait_timeout_probe(igc_stream_t stream);
 
+/*
+ * igc_plan_gemm -- the schedule a GEMM call would run with, computed on the
+ * host by the decisions the launch makes (no device work; with clusters > 0 no
+ * GPU is needed).
+ *
+ *  op        IGC_PLAN_GEMM_F16, IGC_PLAN_GEMM_BF16 or IGC_PLAN_GEMM_S8 (gemm_f16,
+ *            gemm_bf16, gemm_s8_zp / gemm_s8_zp_run / gemm_s8_zp_dequant).
+ *  M, N, K   the problem (all >= 1).
+ *  clusters  CTA pairs that run at once (76 on GB300), or <= 0 for the current
+ *            device's.
+ *  out       int32[8], written: [0] tile width (columns of B per CTA pair),
+ *            [1] pipeline stage depth in k (64 or 128), [2] m-tiles of 256 rows,
+ *            [3] n-tiles, [4] first column-half unit (= tiles when the last
+ *            round is not split), [5] work units, [6] CTAs launched, [7] leading
+ *            units per CTA pair whose operand panels are prefetched into L2.
+ *  The current igc_set_tile_width / igc_set_stage_depth overrides apply.
+ *  Returns IGC_OK, IGC_ERR_INVALID_ARG (null out, size < 1, unknown op),
+ *  IGC_ERR_UNSUPPORTED (sizes beyond 2^31 - 1) or a device error when clusters
+ *  <= 0 and no usable device is present.
+ */
+#define IGC_PLAN_GEMM_F16 0
+#define IGC_PLAN_GEMM_BF16 1
+#define IGC_PLAN_GEMM_S8 2
+int igc_plan_gemm(int op, int64_t M, int64_t N, int64_t K, int clusters, int32_t *out);
+
 /* Library version, "major.minor.patch". */
 const char *igc_version(void);
 
