@@ -25,14 +25,18 @@
 // memory, and receives its 128 x BN accumulator in its own tensor memory.
 // Warp roles in each CTA (384 threads, three warpgroups):
 //   warp 0      TMA producer: its CTA's halves of A and B into a ring of
-//               128-deep stages (two 128-byte swizzle atoms per operand); both
+//               128-deep stages (two 128-byte swizzle atoms per operand; 64-deep
+//               stages, twice as many, for GEMMs of one or two rounds); both
 //               CTAs' copies complete on the leader CTA's `full[s]` barrier.
 //   warp 1      tensor-memory owner; in the leader CTA also the MMA issuer: 8 x
-//               tcgen05.mma per stage, tcgen05.commit multicast to both CTAs frees
+//               tcgen05.mma per stage (4 when 64-deep), tcgen05.commit multicast
+//               to both CTAs frees
 //               ring stages (`empty[s]`) and hands finished accumulators to both
 //               epilogues (`tfull[a]`).  Warps 0 and 1 run their loops converged;
 //               lane 0 issues.
-//   warps 2-3   idle (their warpgroup gives registers to the epilogue).
+//   warps 2-3   GEMMs: L2 prefetch of the first rounds' operand panels, paced by
+//               the producer (convolutions: idle); their warpgroup gives registers
+//               to the epilogue.
 //   warps 4-11  epilogue: tcgen05.ld of their lane quadrant / column half, fused
 //               output math, outputs staged in 128-byte-swizzled shared memory and
 //               written by TMA bulk tensor stores (direct stores for outputs TMA
@@ -41,7 +45,8 @@
 // Two accumulators (2 x BN of the 512 TMEM columns) let the epilogue of one
 // tile overlap the main loop of the next.  The persistent schedule walks tiles
 // in groups of 8 m-tiles; when its last round would fill at most half of the
-// CTA pairs, that round's tiles run as two BN/2-wide column halves.
+// CTA pairs, that round's tiles run as two BN/2-wide column halves (at BN = 256
+// on a four-stage ring laid over the three main stages, tail_slot).
 //
 // The integer modes accumulate in chunks that fp32 holds exactly: products of
 // the shifted operands are integers of magnitude <= 2^14, so every partial sum
@@ -73,7 +78,7 @@ constexpr int BK = 64;         // 64 fp16 = one 128-byte swizzle row (one TMA bo
 constexpr int kAtoms = 2;      // swizzle atoms along k per pipeline stage (default)
 constexpr int KS = BK * kAtoms;  // k depth of one default pipeline stage (8 MMAs of k = 16)
 constexpr int kEpiWarps = 8;
-// Three warpgroups: warps 0-3 (TMA producer, MMA issuer / TMEM owner, two idle)
+// Three warpgroups: warps 0-3 (TMA producer, MMA issuer / TMEM owner, two prefetch)
 // and two epilogue warpgroups (warps 4-11).  After set-up the first warpgroup
 // gives registers to the epilogue ones (setmaxnreg): kRegsLow + 2 kRegsHigh
 // warpgroup shares = 56 * 128 + 216 * 256 = 62464 registers, which fits the
