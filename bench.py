@@ -365,7 +365,16 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
     ms = t_ms(lambda: igc.gemm_s8_zp_dequant(Aq, Bq, zA_row=zA, scale_row=srow, scale_col=scol,
                                              bias=bias, Y=Y, workspace=ws))
     out["gemm_s8_zp_dequant_8192^3_f32_out"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
-    del Aq, Bq, Y, ws
+    # the step's int8 GEMM through the warp-level (mma.sync) path instead of tcgen05
+    C8w = torch.empty((8192, 8192), dtype=torch.int8, device=device)
+    old_path = igc.igc_set_int8_path(igc.INT8_PATH_MMA_SYNC)
+    try:
+        ms = t_ms(lambda: igc.gemm_s8_zp(Aq, Bq, zA_row=zA, C8=C8w, scale_col=scol,
+                                         workspace=ws))
+    finally:
+        igc.igc_set_int8_path(old_path)
+    out["gemm_s8_zp_8192^3_mma_sync_path"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
+    del Aq, Bq, Y, ws, C8w
     # int8 convolution on the layer shape: x uint8 NHWC 256x14x14x256, w int8 512x3x3x256
     x8 = t(synth.uniform_int(43, 6, (256, 14, 14, 256), 0, 255, np.uint8))
     w8 = t(synth.uniform_int(43, 7, (512, 3, 3, 256), -127, 127, np.int8))

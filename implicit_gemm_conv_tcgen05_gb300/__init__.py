@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
             L.igc_set_tile_width.restype = i32
             L.igc_set_stage_depth.argtypes = [i32]
             L.igc_set_stage_depth.restype = i32
+            L.igc_set_int8_path.argtypes = [i32]
+            L.igc_set_int8_path.restype = i32
             L.igc_plan_gemm.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int32)]
             L.igc_plan_gemm.restype = i32
             L.igc_debug_wait_timeout_probe.argtypes = [vp]
@@ -179,6 +181,13 @@ def igc_set_tile_width(bn: int) -> int:
 
 def igc_set_stage_depth(k: int) -> int:
     return int(lib().igc_set_stage_depth(int(k)))
+
+
+INT8_PATH_TCGEN05, INT8_PATH_MMA_SYNC = 0, 1
+
+
+def igc_set_int8_path(path: int) -> int:
+    return int(lib().igc_set_int8_path(int(path)))
 
 
 PLAN_GEMM_F16, PLAN_GEMM_BF16, PLAN_GEMM_S8 = 0, 1, 2

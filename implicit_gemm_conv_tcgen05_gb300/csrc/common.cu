@@ -20,6 +20,7 @@ __device__ unsigned long long g_status_word;
 std::atomic<unsigned long long> g_wait_limit{2000000000ull};
 std::atomic<int> g_tile_width{0};  // 0: chosen per problem
 std::atomic<int> g_stage_depth{0};  // 0: chosen per problem
+std::atomic<int> g_int8_path{0};    // 0: tcgen05, 1: mma.sync
 std::atomic<unsigned long long> g_last_status{0};
 
 struct DeviceSlot {
@@ -123,6 +124,8 @@ int tile_width_override() { return g_tile_width.load(); }
 
 int stage_depth_override() { return g_stage_depth.load(); }
 
+int int8_path_override() { return g_int8_path.load(); }
+
 int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                     uint32_t box_rows) {
@@ -207,6 +210,11 @@ int igc_set_tile_width(int bn) {
 int igc_set_stage_depth(int k) {
   if (k != 0 && k != 64 && k != 128) return -1;
   return igc::g_stage_depth.exchange(k);
+}
+
+int igc_set_int8_path(int path) {
+  if (path != IGC_INT8_PATH_TCGEN05 && path != IGC_INT8_PATH_MMA_SYNC) return -1;
+  return igc::g_int8_path.exchange(path);
 }
 
 uint64_t igc_set_wait_limit_ns(uint64_t limit_ns) {

@@ -236,6 +236,23 @@ extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_
   if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
   if (C32 == nullptr && C8 == nullptr) return IGC_ERR_INVALID_ARG;
   if ((C32 != nullptr && ldc32 < N) || (C8 != nullptr && ldc8 < N)) return IGC_ERR_INVALID_ARG;
+  if (K > 0 && int8_path_override() == IGC_INT8_PATH_MMA_SYNC) {
+    if (A == nullptr || Bt == nullptr || lda < K || ldb < K) return IGC_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(Bt) || lda % 16 != 0 || ldb % 16 != 0)
+      return IGC_ERR_MISALIGNED;
+    const WsLayout l = ws_layout(M, N, K);
+    rc = check_workspace(workspace, workspace_bytes, l);
+    if (rc != IGC_OK) return rc;
+    DeviceInfo dev;
+    rc = current_device(&dev);
+    if (rc != IGC_OK) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return imma_gemm_s8_zp(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), A,
+                           a_signed, lda, Bt, b_signed, ldb, zA, zA_row, zB, zB_col, C32, ldc32,
+                           C8, ldc8, scale, scale_col, reinterpret_cast<int32_t*>(ws + l.ra_off),
+                           reinterpret_cast<int32_t*>(ws + l.cb_off),
+                           reinterpret_cast<cudaStream_t>(stream));
+  }
   if (K > 0) {
     if (A == nullptr || Bt == nullptr) return IGC_ERR_INVALID_ARG;
     rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,

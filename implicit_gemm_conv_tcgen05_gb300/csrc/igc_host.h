@@ -28,6 +28,14 @@ unsigned long long* status_word();
 unsigned long long wait_limit_ns();
 int tile_width_override();  // 0, or the tile width set by igc_set_tile_width
 int stage_depth_override();  // 0, or the stage depth set by igc_set_stage_depth
+int int8_path_override();    // 0 (tcgen05) or 1 (mma.sync), set by igc_set_int8_path
+
+// gemm_s8_zp on the warp-level (mma.sync) tensor path; arguments checked by the caller
+int imma_gemm_s8_zp(int M, int N, int K, const void* A, int a_signed, long long lda,
+                    const void* Bt, int b_signed, long long ldb, int32_t zA,
+                    const int32_t* zA_row, int32_t zB, const int32_t* zB_col, int32_t* C32,
+                    long long ldc32, int8_t* C8, long long ldc8, float scale,
+                    const float* scale_col, int32_t* rA, int32_t* cB, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled / cuTensorMapEncodeIm2col through the runtime's
 // driver entry point (the library does not link libcuda directly).

@@ -365,6 +365,24 @@ int igc_set_tile_width(int bn);
 int igc_set_stage_depth(int k);
 
 /*
+ * Selects the tensor path of gemm_s8_zp (the combined call; the prepare / run
+ * split, gemm_s8_zp_dequant and the convolutions always use tcgen05) for calls
+ * made after this one:
+ *  IGC_INT8_PATH_TCGEN05 (default): exact integers on the tcgen05 fp16 pipe
+ *    after the operand pre-pass (gemm_s8_zp above).
+ *  IGC_INT8_PATH_MMA_SYNC: warp-level mma.sync m16n8k32 on the raw uint8 /
+ *    int8 operands into int32 registers, raw row / column sums in the
+ *    workspace's sum slots, the same correction and requantisation ([P1] §2.3's
+ *    IMMA form).  Bit-identical results; far slower on sm_103a, whose
+ *    warp-level integer MMA rate is a fraction of the tcgen05 fp16 rate.
+ * Returns the previous setting, or -1 (and changes nothing) for any other
+ * value.  Process-wide.
+ */
+#define IGC_INT8_PATH_TCGEN05 0
+#define IGC_INT8_PATH_MMA_SYNC 1
+int igc_set_int8_path(int path);
+
+/*
  * Diagnostic: launches one CTA that waits on an mbarrier nothing ever
  * completes, with the current wait limit, and returns.  The wait gives up
  * after the limit and records IGC_ERR_DEVICE_TIMEOUT for

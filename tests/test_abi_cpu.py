@@ -18,6 +18,7 @@ def test_library_loads_and_exports_every_declared_symbol():
                 "conv2d_nhwc_s8_zp", "conv2d_nhwc_s8_zp_workspace_size", "conv2d_nhwc_f16_implicit",
                 "igc_status_string", "igc_check_device_status", "igc_last_device_status",
                 "igc_set_wait_limit_ns", "igc_set_tile_width", "igc_set_stage_depth",
+                "igc_set_int8_path", "igc_plan_gemm",
                 "igc_debug_wait_timeout_probe",
                 "igc_version"}
     assert expected <= set(names)
@@ -106,6 +107,12 @@ def test_tile_width_setter_roundtrip():
     assert igc.igc_set_tile_width(96) == -1          # not a built width: unchanged
     assert igc.igc_set_tile_width(128) == 224
     assert igc.igc_set_tile_width(0) == 128
+
+
+def test_int8_path_setter_roundtrip():
+    assert igc.igc_set_int8_path(igc.INT8_PATH_MMA_SYNC) == igc.INT8_PATH_TCGEN05
+    assert igc.igc_set_int8_path(2) == -1            # no such path: unchanged
+    assert igc.igc_set_int8_path(igc.INT8_PATH_TCGEN05) == igc.INT8_PATH_MMA_SYNC
 
 
 def test_stage_depth_setter_roundtrip():
