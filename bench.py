@@ -620,6 +620,27 @@ def oracle_sample(w3, w4, w5, frac_log2: int):
     return ops, dt, desc
 
 
+def cpu_model() -> str:
+    """The host CPU's model as the kernel reports it (x86 'model name', or the Arm
+    implementer / part numbers), else the machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        info = ""
+    fields = {}
+    for line in info.splitlines():
+        k, _, v = line.partition(":")
+        fields.setdefault(k.strip(), v.strip())
+    if fields.get("model name"):
+        return fields["model name"]
+    if fields.get("CPU implementer"):
+        return (f"{platform.machine()} implementer {fields['CPU implementer']} "
+                f"part {fields.get('CPU part', '?')}")
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(w3, w4, w5, target_s: float = 15.0):
     import oracle
     k = 10
@@ -629,7 +650,7 @@ def cpu_baseline(w3, w4, w5, target_s: float = 15.0):
         k = max(1, k - max(1, int(np.floor(np.log2(target_s / max(dt, 1e-3))))))
         ops, dt, desc = oracle_sample(w3, w4, w5, k)
     return {"value": ops / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(),
-            "kind": "oracle", "sample": desc, "seconds": dt}
+            "cpu_model": cpu_model(), "kind": "oracle", "sample": desc, "seconds": dt}
 
 
 def run_reference(args):
@@ -659,8 +680,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64/int64 (oracle)",
         "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": WORKLOAD, "sample_per_step": desc, "ops_per_sample": ops},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -724,7 +745,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
