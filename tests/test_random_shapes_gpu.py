@@ -107,3 +107,81 @@ def test_random_conv_f16_and_s8(N, H, W, C, K, R, S, pad, stride):
                                           pad=pad, stride=stride, scale_k=scale_k)
     assert np.array_equal(host(g32), o32)
     assert np.array_equal(host(g8), o8)
+
+
+def test_random_sweep_exact_small_integers():
+    """A seeded sweep of 150 more cases drawn across operations and forced schedule
+    choices (tile width, stage depth, the int8 tensor path): fp16 GEMMs and
+    convolutions on small-integer operands, whose sums are exact in fp32, compared
+    with the oracle bit for bit; int8 GEMMs bit for bit."""
+    rng = np.random.default_rng(20261203)
+    done = 0
+    while done < 150:
+        kind = int(rng.integers(0, 3))
+        if kind == 0:
+            M, N, K = int(rng.integers(1, 3000)), int(rng.integers(1, 3000)), 8 * int(rng.integers(1, 700))
+            if M * N * K > 3e9:
+                continue
+            A = rng.integers(-2, 3, size=(M, K)).astype(np.float16)
+            Bt = rng.integers(-2, 3, size=(N, K)).astype(np.float16)
+            w, d = int(rng.choice([0, 0, 0, 128, 224, 256])), int(rng.choice([0, 0, 64, 128]))
+            old_w, old_d = igc.igc_set_tile_width(w), igc.igc_set_stage_depth(d)
+            try:
+                C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+                igc.gemm_f16(dev(A), dev(Bt), C)
+                check_device_ok()
+            finally:
+                igc.igc_set_tile_width(old_w)
+                igc.igc_set_stage_depth(old_d)
+            ref, _ = oracle.gemm_f16(A, Bt)
+            assert np.array_equal(host(C), ref.astype(np.float32)), ("f16", M, N, K, w, d)
+        elif kind == 1:
+            M, N, K = int(rng.integers(1, 2500)), int(rng.integers(1, 2500)), 16 * int(rng.integers(1, 300))
+            if M * N * K > 3e9:
+                continue
+            A = rng.integers(0, 256, size=(M, K)).astype(np.uint8)
+            Bt = rng.integers(-128, 128, size=(N, K)).astype(np.int8)
+            zA = rng.integers(0, 256, size=M).astype(np.int32)
+            zB = int(rng.integers(-128, 128))
+            sc = rng.uniform(1e-6, 1e-3, size=N).astype(np.float32)
+            w, path = int(rng.choice([0, 0, 128, 256])), int(rng.choice([0, 0, 0, 1]))
+            old_w, old_p = igc.igc_set_tile_width(w), igc.igc_set_int8_path(path)
+            try:
+                C32 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+                C8 = torch.empty((M, N), dtype=torch.int8, device="cuda")
+                igc.gemm_s8_zp(dev(A), dev(Bt), zA_row=dev(zA), zB=zB, C32=C32, C8=C8,
+                               scale_col=dev(sc))
+                check_device_ok()
+            finally:
+                igc.igc_set_tile_width(old_w)
+                igc.igc_set_int8_path(old_p)
+            o32, o8, _, _ = oracle.gemm_s8_zp(A, Bt, a_signed=0, b_signed=1, zA_row=zA, zB=zB,
+                                              scale_col=sc)
+            assert np.array_equal(host(C32), o32) and np.array_equal(host(C8), o8), \
+                ("s8", M, N, K, w, path)
+        else:
+            n, H, W = int(rng.integers(1, 5)), int(rng.integers(3, 20)), int(rng.integers(3, 20))
+            C, K = 8 * int(rng.integers(1, 40)), 8 * int(rng.integers(1, 64))
+            R, S = int(rng.integers(1, 6)), int(rng.integers(1, 6))
+            if R > H or S > W:
+                continue
+            pad = (int(rng.integers(0, R)), int(rng.integers(0, S)))
+            stride = (int(rng.integers(1, 3)), int(rng.integers(1, 3)))
+            x = rng.integers(-2, 3, size=(n, H, W, C)).astype(np.float16)
+            wt = rng.integers(-1, 2, size=(K, R, S, C)).astype(np.float16)
+            d, w = int(rng.choice([0, 0, 64])), int(rng.choice([0, 0, 128, 224, 256]))
+            old_d, old_w = igc.igc_set_stage_depth(d), igc.igc_set_tile_width(w)
+            P = (H + 2 * pad[0] - R) // stride[0] + 1
+            Q = (W + 2 * pad[1] - S) // stride[1] + 1
+            try:
+                y = torch.empty((n, P, Q, K), dtype=torch.float16, device="cuda")
+                y32 = torch.empty((n, P, Q, K), dtype=torch.float32, device="cuda")
+                igc.conv2d_nhwc_f16_implicit(dev(x), dev(wt), y, y32, pad=pad, stride=stride)
+                check_device_ok()
+            finally:
+                igc.igc_set_stage_depth(old_d)
+                igc.igc_set_tile_width(old_w)
+            ref, _ = oracle.conv2d_nhwc_f16(x, wt, pad=pad, stride=stride)
+            assert np.array_equal(host(y32), ref.astype(np.float32)), \
+                ("conv", n, H, W, C, K, R, S, pad, stride, d, w)
+        done += 1
