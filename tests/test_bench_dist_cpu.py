@@ -1,6 +1,6 @@
-"""The multi-rank bookkeeping of bench.py on CPU: two gloo ranks, each with its
-own step time, must agree on the slowest one; the reference arm runs on rank 0
-only and the other ranks exit without work."""
+"""bench.py's host logic on CPU: two gloo ranks, each with its own step time,
+must agree on the slowest one; the reference arm runs on rank 0 only and the
+other ranks exit without work; the traffic key and the CPU description."""
 
 import os
 import subprocess
@@ -53,3 +53,27 @@ def test_reference_arm_non_zero_rank_exits_quietly():
                        text=True, timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def _bench():
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def test_traffic_key_ignores_comments_but_not_code():
+    """The ncu traffic figures are keyed by a digest of the kernel sources' code:
+    editing a comment keeps them, editing code drops them (the roofline's traffic
+    then reads null until a new capture)."""
+    bench = _bench()
+    src = {"k.cu": "// note\nint f() { return 1; }  // trailing\n/* block */\n"}
+    base = bench.csrc_digest(src)
+    assert bench.csrc_digest({"k.cu": "// other words\nint f() { return 1; }\n"}) == base
+    assert bench.csrc_digest({"k.cu": "int f() { return 2; }\n"}) != base
+    assert bench.csrc_digest({"k.cu": src["k.cu"], "new.cu": "int g();\n"}) != base
+
+
+def test_cpu_model_is_reported():
+    bench = _bench()
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
