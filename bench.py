@@ -47,6 +47,26 @@ OPS = {
     "gemm_s8_zp_8192": 2.0 * 8192 ** 3,
 }
 OPS_PER_STEP = sum(OPS.values())
+# compulsory HBM bytes of each operation at its configuration (inputs read once,
+# outputs written once), for the per-shape roofline max(work / peak, bytes / HBM)
+BYTES = {
+    "gemm_f16_256": 2 * 256 * 256 * 2 + 256 * 256 * 4,
+    "gemm_s8_zp_1024": 2 * 1024 * 1024 + 1024 * 1024 * (4 + 1),
+    "gemm_f16_4096": 3 * 4096 * 4096 * 2,
+    "conv3x3_256x14x14x256_512": 2 * (256 * 14 * 14 * 256 + 512 * 9 * 256 + 256 * 14 * 14 * 512),
+    "gemm_s8_zp_8192": 3 * 8192 * 8192 + 8192 * (4 + 4),
+}
+
+
+def roofline_fields(ops: float, nbytes: float, ms: float, peak_tflops: float, hbm_gbs: float):
+    """Achieved HBM rate of the compulsory bytes, the roofline time max(work / tensor
+    peak, bytes / HBM) and the fraction of it that the measured time reaches."""
+    t_tensor = ops / (peak_tflops * 1e12)
+    t_hbm = nbytes / (hbm_gbs * 1e9) if hbm_gbs else 0.0
+    t_roof = max(t_tensor, t_hbm)
+    return {"gbs": nbytes / (ms * 1e-3) / 1e9, "roofline_us": t_roof * 1e6,
+            "roofline_frac": t_roof / (ms * 1e-3),
+            "roofline_bound": "tensor" if t_tensor >= t_hbm else "hbm"}
 FALLBACK_TFLOPS = 1900.0
 KERNEL_SOURCES = os.path.join(ROOT, "implicit_gemm_conv_tcgen05_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
@@ -421,7 +441,8 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
     C1 = torch.empty((256, 256), dtype=torch.float32, device=device)
     ms = t_ms(lambda: igc.gemm_f16(A1, B1, C1))
     out["gemm_f16_256^3_f32_out"] = {"ms": ms, "tflops": 2 * 256 ** 3 / ms / 1e9,
-                                     "gbs": (2 * 2 * 256 * 256 + 4 * 256 * 256) / ms / 1e6}
+                                     **roofline_fields(2.0 * 256 ** 3, BYTES["gemm_f16_256"], ms,
+                                                       peak_tflops, hbm_gbs)}
     w2 = synth.workload(2)
     A2, B2 = t(w2["A"]), t(w2["Bt"])
     C32 = torch.empty((1024, 1024), dtype=torch.int32, device=device)
@@ -431,7 +452,8 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
     ms = t_ms(lambda: igc.gemm_s8_zp(A2, B2, zA=128, zB=121, C32=C32, C8=C8,
                                      scale=w2["scale"], workspace=ws2))
     out["gemm_s8_zp_1024^3_c32_c8"] = {"ms": ms, "tops": 2 * 1024 ** 3 / ms / 1e9,
-                                       "gbs": (2 * 1024 * 1024 + 5 * 1024 * 1024) / ms / 1e6}
+                                       **roofline_fields(2.0 * 1024 ** 3, BYTES["gemm_s8_zp_1024"],
+                                                         ms, peak_tflops, hbm_gbs)}
     # the same two calls as 100 back-to-back launches replayed from a CUDA graph
     # (no host launch cost; inputs stay in L2 between the launches)
     ms = graph_ms(lambda: igc.gemm_f16(A1, B1, C1))
@@ -530,9 +552,11 @@ def run_ours(args, rank, world, local_rank):
                               "prepass_ms": prep_ms, "gemm_kernel_ms": run_ms,
                               "gemm_kernel_tops": OPS["gemm_s8_zp_8192"] / run_ms / 1e9},
     }
-    for v, col in zip(per_shape.values(), (seg[:, 0], seg[:, 1], int8_seg)):
+    for (key, v), col in zip(zip(("gemm_f16_4096", "conv3x3_256x14x14x256_512", "gemm_s8_zp_8192"),
+                                 per_shape.values()), (seg[:, 0], seg[:, 1], int8_seg)):
         t = v.get("tflops", v.get("tops"))
         v["frac_of_peak"] = t / peak_burst
+        v.update(roofline_fields(OPS[key], BYTES[key], v["ms"], peak_burst, hbm))
         v["ms_median"] = float(np.median(col))
         v["ms_min"] = float(col.min())
     # Share of the int8 outputs that the requantisation clamped to -128 or 127 (with

@@ -77,3 +77,16 @@ def test_traffic_key_ignores_comments_but_not_code():
 def test_cpu_model_is_reported():
     bench = _bench()
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_roofline_fields():
+    bench = _bench()
+    # 1 TFLOP at 1000 TF/s = 1 ms; 1 GB at 1000 GB/s = 1 ms; measured 2 ms -> half
+    r = bench.roofline_fields(1e12, 1e9, 2.0, 1000.0, 1000.0)
+    assert abs(r["roofline_us"] - 1000.0) < 1e-6 and abs(r["roofline_frac"] - 0.5) < 1e-12
+    assert abs(r["gbs"] - 500.0) < 1e-9
+    # four times the bytes: the HBM term binds
+    r = bench.roofline_fields(1e12, 4e9, 8.0, 1000.0, 1000.0)
+    assert r["roofline_bound"] == "hbm" and abs(r["roofline_frac"] - 0.5) < 1e-12
+    # no HBM figure: only the tensor term
+    assert bench.roofline_fields(1e12, 4e9, 2.0, 1000.0, 0.0)["roofline_bound"] == "tensor"
