@@ -3,6 +3,7 @@ exports every function include/igc.h declares, and rejects bad arguments on
 the host before touching a device."""
 
 import ctypes
+import os
 import re
 
 import pytest
@@ -120,3 +121,30 @@ def test_stage_depth_setter_roundtrip():
     assert igc.igc_set_stage_depth(96) == -1         # not a built depth: unchanged
     assert igc.igc_set_stage_depth(128) == 64
     assert igc.igc_set_stage_depth(0) == 128
+
+
+def test_header_is_c99_and_links_from_c(tmp_path):
+    """A C99 program includes include/igc.h, links libigc.so and calls the host-only
+    entry points (no GPU): the boundary is a plain C ABI."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    lib = igc.lib()._name
+    src = tmp_path / "use_igc.c"
+    src.write_text(
+        '#include <string.h>\n#include "igc.h"\n'
+        "int main(void) {\n"
+        "  int32_t out[8];\n"
+        "  if (igc_plan_gemm(IGC_PLAN_GEMM_F16, 4096, 4096, 4096, 76, out) != IGC_OK) return 1;\n"
+        "  if (out[0] != 256 || out[4] != 228 || out[5] != 284) return 2;\n"
+        "  if (gemm_s8_zp_workspace_size(-1, 1, 1) != 0) return 3;\n"
+        "  if (strlen(igc_status_string(IGC_ERR_MISALIGNED)) == 0) return 4;\n"
+        "  if (igc_set_tile_width(96) != -1) return 5;\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "use_igc"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), lib, "-o", str(exe),
+                    f"-Wl,-rpath,{os.path.dirname(lib)}"], check=True)
+    assert subprocess.run([str(exe)]).returncode == 0
