@@ -499,3 +499,80 @@ def test_conv_s8_delta_kernel_and_requant():
     assert np.array_equal(y32, x.astype(np.int32) - 100)
     assert np.array_equal(y8, np.array([[oracle.requant(int(v), 0.5) for v in row]
                                         for row in y32.reshape(-1, 8)], np.int8).reshape(y8.shape))
+
+
+# ---------------------------------------------------------------------------
+# the acceptance test of every fp16 / bf16 parity check
+# ---------------------------------------------------------------------------
+# oracle.fp16_accept decides "|gpu - exact| <= rel * sum_k |a_ik b_kj|" per element
+# (the stated tolerance of the floating-point GEMM and convolution, applied to the
+# GEMM definition of the GEMM page, §4.1).  Hand-built cases: an error exactly at
+# the bound is accepted and the next representable value beyond it is not, on
+# either side of the exact value and in float32 and float64; NaN / inf results
+# are rejected wherever they sit; an element whose |a b| sum is 0 must be exactly
+# 0; a custom rel is honoured; one bad element among good ones rejects the lot.
+
+def test_fp16_accept_error_at_the_bound_is_accepted_and_just_beyond_is_not():
+    sabs = np.array([500.0, 1000.0, 250.0])          # bounds 1.0, 2.0, 0.5 (exact)
+    # ref +- bound and its neighbours lie within a factor of two of ref, so every
+    # error below is computed exactly in float64 (Sterbenz)
+    ref = np.array([3.0, -7.0, 2.0])
+    bound = 2e-3 * sabs
+    assert bound.tolist() == [1.0, 2.0, 0.5]
+    for dt in (np.float32, np.float64):
+        for sign in (1.0, -1.0):
+            at = (ref + sign * bound).astype(dt)
+            assert np.array_equal(at.astype(np.float64), ref + sign * bound)  # representable
+            ok, worst = oracle.fp16_accept(at, ref, sabs)
+            assert ok and worst == 1.0
+            for i in range(3):
+                beyond = at.copy()
+                beyond[i] = np.nextafter(at[i], dt(sign * np.inf))
+                ok, worst = oracle.fp16_accept(beyond, ref, sabs)
+                assert not ok and worst > 1.0, (dt, sign, i)
+
+
+def test_fp16_accept_rejects_nan_and_inf_results():
+    ref = np.zeros(4)
+    sabs = np.full(4, 1e30)                       # a bound no finite error reaches
+    for bad in (np.nan, np.inf, -np.inf):
+        for i in range(4):
+            g = np.zeros(4, np.float32)
+            g[i] = bad
+            ok, _ = oracle.fp16_accept(g, ref, sabs)
+            assert not ok, (bad, i)
+    ok, _ = oracle.fp16_accept(np.zeros(4, np.float16), ref, sabs)
+    assert ok
+
+
+def test_fp16_accept_zero_abs_sum_demands_exact_zero():
+    ref = np.array([0.0, 0.0])
+    sabs = np.array([0.0, 5.0])
+    ok, worst = oracle.fp16_accept(np.array([0.0, 0.01], np.float32), ref, sabs)
+    assert ok and worst <= 1.0
+    for tiny in (np.float32(1e-45), np.float32(-1e-45), np.float16(6e-8)):
+        g = np.array([tiny, 0.0]).astype(np.float32)
+        ok, worst = oracle.fp16_accept(g, ref, sabs)
+        assert not ok and worst == np.inf
+
+
+def test_fp16_accept_honours_rel():
+    ref = np.array([1.0])
+    sabs = np.array([1000.0])
+    g = np.array([1.0 + 5.0])                     # 2.5 x the default bound of 2.0
+    assert not oracle.fp16_accept(g, ref, sabs)[0]
+    ok, worst = oracle.fp16_accept(g, ref, sabs, rel=5e-3)   # bound 5.0: at it
+    assert ok and worst == 1.0
+    assert not oracle.fp16_accept(g, ref, sabs, rel=4e-3)[0]
+
+
+def test_fp16_accept_one_bad_element_rejects_the_array():
+    rng = np.random.default_rng(7)
+    sabs = rng.uniform(1.0, 100.0, (64, 64))
+    ref = rng.normal(size=(64, 64))
+    g = ref + 0.5 * 2e-3 * sabs * rng.uniform(-1.0, 1.0, (64, 64))
+    ok, worst = oracle.fp16_accept(g, ref, sabs)
+    assert ok and worst <= 0.5
+    g[17, 41] = ref[17, 41] + 1.5 * 2e-3 * sabs[17, 41]
+    ok, worst = oracle.fp16_accept(g, ref, sabs)
+    assert not ok and abs(worst - 1.5) < 1e-9
