@@ -353,25 +353,6 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
     ms = t_ms(lambda: igc.gemm_bf16(A, B, C))
     out["gemm_bf16_4096^3"] = {"ms": ms, "tflops": 2 * 4096 ** 3 / ms / 1e9}
     del A, B, C
-    # the vendor library's fp16 GEMM on the step's 4096^3 inputs (context only)
-    A = t(synth.normal_f16(synth.seed_for(3), synth.TID_A, (4096, 4096)))
-    B = t(synth.normal_f16(synth.seed_for(3), synth.TID_B, (4096, 4096)))
-    C = torch.empty((4096, 4096), dtype=torch.float16, device=device)
-    ms = t_ms(lambda: torch.matmul(A, B.t(), out=C))
-    out["context_torch_matmul_f16_4096^3"] = {"ms": ms, "tflops": 2 * 4096 ** 3 / ms / 1e9}
-    del A, B, C
-    # the vendor library's fp16 convolution (cuDNN through torch, algorithm autotuned)
-    # on the step's convolution inputs, NHWC memory (context only)
-    w4 = synth.workload(4)
-    xc = t(w4["x"]).permute(0, 3, 1, 2)  # NCHW view of the NHWC tensor (channels_last)
-    wc = t(w4["w"]).permute(0, 3, 1, 2)  # K x C x R x S view of the KRSC tensor
-    prev_bench = torch.backends.cudnn.benchmark
-    torch.backends.cudnn.benchmark = True
-    ms = t_ms(lambda: torch.nn.functional.conv2d(xc, wc, padding=1))
-    torch.backends.cudnn.benchmark = prev_bench
-    out["context_cudnn_conv3x3_256x14x14x256->512"] = {
-        "ms": ms, "tflops": OPS["conv3x3_256x14x14x256_512"] / ms / 1e9}
-    del xc, wc, w4
     # int8 GEMM 8192^3 with the dequantised fp32 output (dequantise + bias fused)
     w5 = synth.workload(5)
     Aq, Bq = t(w5["A"]), t(w5["Bt"])
@@ -414,15 +395,12 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
     out["conv3x3_stride2_256x28x28x128->256"] = {
         "ms": ms, "tflops": 2.0 * 256 * 14 * 14 * 256 * 9 * 128 / ms / 1e9}
     del xs, wsx, ys
-    # fp16 GEMM 8192^3 (the size of the measured bf16 peak), and the vendor library's
-    # GEMM on the same inputs in the same run as context (not part of the product path)
+    # fp16 GEMM 8192^3 (the size of the measured bf16 peak)
     A8 = t(synth.normal_f16(46, 1, (8192, 8192)))
     B8 = t(synth.normal_f16(46, 2, (8192, 8192)))
     C8h = torch.empty((8192, 8192), dtype=torch.float16, device=device)
     ms = t_ms(lambda: igc.gemm_f16(A8, B8, C8h))
     out["gemm_f16_8192^3"] = {"ms": ms, "tflops": 2 * 8192 ** 3 / ms / 1e9}
-    ms = t_ms(lambda: torch.matmul(A8, B8.t(), out=C8h))
-    out["context_torch_matmul_f16_8192^3"] = {"ms": ms, "tflops": 2 * 8192 ** 3 / ms / 1e9}
     del A8, B8, C8h
     # skinny fp16 GEMMs: M x 8192 x 8192 (B dominates the bytes)
     Bk = t(synth.normal_f16(45, 2, (8192, 8192)))
@@ -619,8 +597,7 @@ def run_ours(args, rank, world, local_rank):
         result["extras"] = extras_measure(device, peak_burst, hbm)
         result["extras_note"] = ("rows beyond the step, each timed alone (L2 flushed, median of "
                                  "10; *_graph100 rows: per-call time of 100 launches replayed "
-                                 "from a CUDA graph, L2 warm; context_* rows time the vendor "
-                                 "library on the same inputs, not this code); not part of value")
+                                 "from a CUDA graph, L2 warm); not part of value")
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w3, w4, w5, target_s=args.cpu_seconds)

@@ -19,6 +19,7 @@ import threading
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_PKG)
 HEADER = os.path.join(_ROOT, "include", "igc.h")
+DEBUG_HEADER = os.path.join(_ROOT, "include", "igc_debug.h")
 
 IGC_OK = 0
 IGC_ERR_INVALID_ARG = 1
@@ -115,9 +116,10 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def declared_functions() -> list[str]:
-    """Names of the functions include/igc.h declares."""
-    with open(HEADER) as f:
+def declared_functions(header: str = HEADER) -> list[str]:
+    """Names of the functions a header declares (include/igc.h by default;
+    include/igc_debug.h holds the tuning and test hooks)."""
+    with open(header) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) -
@@ -148,15 +150,52 @@ def _check(rc: int, what: str):
         raise IGCError(rc, what)
 
 
-def _rows(t, name, dtype=None):
-    """(rows, cols, row stride in elements) of a 2-D row-major view."""
+def _rows(t, name, dtype=None, shape=None, cuda=True):
+    """(rows, cols, row stride in elements) of a 2-D row-major view; checks the
+    dtype and, when given, the (rows, cols) shape, then (unless cuda is False,
+    for a caller that checks devices last with _require_cuda) the device."""
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError(f"{name} must be a 2-D row-major view with unit inner stride")
     if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise TypeError(f"{name} has dtype {t.dtype}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if cuda:
+        _require_cuda(**{name: t})
     return t.shape[0], t.shape[1], max(t.stride(0), t.shape[1])
+
+
+def _require_cuda(**tensors):
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _vec(v, name, n, dtype):
+    """Checks an optional per-row / per-column vector: dense, `n` elements of
+    `dtype` (its device is checked by the caller's _require_cuda)."""
+    if v is None:
+        return
+    if v.dtype != dtype or v.numel() != n or not v.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} vector of length {n}")
+
+
+def _s8_outputs(C32, C8, M, N):
+    """Row strides of the int8 GEMM's outputs (0 for an absent one), shapes checked."""
+    import torch
+    ldc32 = _rows(C32, "C32", torch.int32, (M, N), cuda=False)[2] if C32 is not None else 0
+    ldc8 = _rows(C8, "C8", torch.int8, (M, N), cuda=False)[2] if C8 is not None else 0
+    return ldc32, ldc8
+
+
+def _s8_operands(A, Bt):
+    """(M, N, K, lda, ldb) of the int8 GEMM's operands, dtypes and K checked."""
+    import torch
+    M, K, lda = _rows(A, "A", (torch.uint8, torch.int8), cuda=False)
+    N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8), cuda=False)
+    if K2 != K:
+        raise ValueError("A and Bt disagree on K")
+    return M, N, K, lda, ldb
 
 
 def status_string(status: int) -> str:
@@ -174,6 +213,9 @@ def igc_check_device_status(stream=None) -> int:
 def igc_last_device_status() -> int:
     return int(lib().igc_last_device_status())
 
+
+# Tuning and test hooks (include/igc_debug.h): thread-local, they force a schedule
+# choice of the calling thread's later calls only.
 
 def igc_set_tile_width(bn: int) -> int:
     return int(lib().igc_set_tile_width(int(bn)))
@@ -231,15 +273,11 @@ def gemm_f16(A, Bt, C=None, C_f32_check=None, stream=None):
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     c_dtype, ldc = IGC_F32, 0
     if C is not None:
-        m, n, ldc = _rows(C, "C", (torch.float16, torch.float32))
-        if (m, n) != (M, N):
-            raise ValueError("C has the wrong shape")
+        ldc = _rows(C, "C", (torch.float16, torch.float32), (M, N))[2]
         c_dtype = IGC_F16 if C.dtype == torch.float16 else IGC_F32
     ldc32 = 0
     if C_f32_check is not None:
-        m, n, ldc32 = _rows(C_f32_check, "C_f32_check", torch.float32)
-        if (m, n) != (M, N):
-            raise ValueError("C_f32_check has the wrong shape")
+        ldc32 = _rows(C_f32_check, "C_f32_check", torch.float32, (M, N))[2]
     rc = lib().gemm_f16(M, N, K, _ptr(A), lda, _ptr(Bt), ldb, _ptr(C), ldc, c_dtype,
                         _ptr(C_f32_check), ldc32, _stream(stream))
     _check(rc, "gemm_f16")
@@ -258,15 +296,11 @@ def gemm_bf16(A, Bt, C=None, C_f32_check=None, stream=None):
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     c_dtype, ldc = IGC_F32, 0
     if C is not None:
-        m, n, ldc = _rows(C, "C", (torch.bfloat16, torch.float32))
-        if (m, n) != (M, N):
-            raise ValueError("C has the wrong shape")
+        ldc = _rows(C, "C", (torch.bfloat16, torch.float32), (M, N))[2]
         c_dtype = IGC_BF16 if C.dtype == torch.bfloat16 else IGC_F32
     ldc32 = 0
     if C_f32_check is not None:
-        m, n, ldc32 = _rows(C_f32_check, "C_f32_check", torch.float32)
-        if (m, n) != (M, N):
-            raise ValueError("C_f32_check has the wrong shape")
+        ldc32 = _rows(C_f32_check, "C_f32_check", torch.float32, (M, N))[2]
     rc = lib().gemm_bf16(M, N, K, _ptr(A), lda, _ptr(Bt), ldb, _ptr(C), ldc, c_dtype,
                          _ptr(C_f32_check), ldc32, _stream(stream))
     _check(rc, "gemm_bf16")
@@ -282,23 +316,12 @@ def gemm_s8_zp(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, C32=None, C8=None,
     """INT8 GEMM with zero points: A (M,K) uint8/int8, Bt (N,K) uint8/int8.
     Outputs C32 (M,N) int32 and/or C8 (M,N) int8.  Returns (C32, C8)."""
     import torch
-    M, K, lda = _rows(A, "A", (torch.uint8, torch.int8))
-    N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8))
-    if K2 != K:
-        raise ValueError("A and Bt disagree on K")
-    ldc32 = ldc8 = 0
-    if C32 is not None:
-        m, n, ldc32 = _rows(C32, "C32", torch.int32)
-        if (m, n) != (M, N):
-            raise ValueError("C32 has the wrong shape")
-    if C8 is not None:
-        m, n, ldc8 = _rows(C8, "C8", torch.int8)
-        if (m, n) != (M, N):
-            raise ValueError("C8 has the wrong shape")
-    for v, name, n_, dt in ((zA_row, "zA_row", M, torch.int32), (zB_col, "zB_col", N, torch.int32),
-                            (scale_col, "scale_col", N, torch.float32)):
-        if v is not None and (v.dtype != dt or v.numel() != n_ or not v.is_contiguous() or not v.is_cuda):
-            raise ValueError(f"{name} must be a contiguous CUDA {dt} vector of length {n_}")
+    M, N, K, lda, ldb = _s8_operands(A, Bt)
+    ldc32, ldc8 = _s8_outputs(C32, C8, M, N)
+    _vec(zA_row, "zA_row", M, torch.int32)
+    _vec(zB_col, "zB_col", N, torch.int32)
+    _vec(scale_col, "scale_col", N, torch.float32)
+    _require_cuda(A=A, Bt=Bt, C32=C32, C8=C8, zA_row=zA_row, zB_col=zB_col, scale_col=scale_col)
     need = gemm_s8_zp_workspace_size(M, N, K)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=A.device)
@@ -317,20 +340,17 @@ def gemm_s8_zp_dequant(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, scale_row=No
     """INT8 GEMM with zero points and a dequantised fp32 output
     Y = ((fp32(C32) * scale_row_i) * scale_col_j) + bias_j.  Returns Y."""
     import torch
-    M, K, lda = _rows(A, "A", (torch.uint8, torch.int8))
-    N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8))
-    if K2 != K:
-        raise ValueError("A and Bt disagree on K")
+    M, N, K, lda, ldb = _s8_operands(A, Bt)
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    m, n, ldy = _rows(Y, "Y", torch.float32)
-    if (m, n) != (M, N):
-        raise ValueError("Y has the wrong shape")
-    for v, name, n_, dt in ((zA_row, "zA_row", M, torch.int32), (zB_col, "zB_col", N, torch.int32),
-                            (scale_row, "scale_row", M, torch.float32),
-                            (scale_col, "scale_col", N, torch.float32), (bias, "bias", N, torch.float32)):
-        if v is not None and (v.dtype != dt or v.numel() != n_ or not v.is_contiguous() or not v.is_cuda):
-            raise ValueError(f"{name} must be a contiguous CUDA {dt} vector of length {n_}")
+    ldy = _rows(Y, "Y", torch.float32, (M, N), cuda=False)[2]
+    _vec(zA_row, "zA_row", M, torch.int32)
+    _vec(zB_col, "zB_col", N, torch.int32)
+    _vec(scale_row, "scale_row", M, torch.float32)
+    _vec(scale_col, "scale_col", N, torch.float32)
+    _vec(bias, "bias", N, torch.float32)
+    _require_cuda(A=A, Bt=Bt, Y=Y, zA_row=zA_row, zB_col=zB_col, scale_row=scale_row,
+                  scale_col=scale_col, bias=bias)
     if workspace is None:
         workspace = torch.empty(max(gemm_s8_zp_workspace_size(M, N, K), 1), dtype=torch.uint8,
                                 device=A.device)
@@ -353,12 +373,12 @@ def gemm_s8_zp_noalloc(A, Bt, zA=0, zA_row=None, zB=0, zB_col=None, C32=None, C8
     its own fixed scratch (IGC_NOALLOC_SCRATCH_BYTES per GPU) instead of a
     workspace.  Calls that overlap on the GPU race on that scratch."""
     import torch
-    M, K, lda = _rows(A, "A", (torch.uint8, torch.int8))
-    N, K2, ldb = _rows(Bt, "Bt", (torch.uint8, torch.int8))
-    if K2 != K:
-        raise ValueError("A and Bt disagree on K")
-    ldc32 = _rows(C32, "C32", torch.int32)[2] if C32 is not None else 0
-    ldc8 = _rows(C8, "C8", torch.int8)[2] if C8 is not None else 0
+    M, N, K, lda, ldb = _s8_operands(A, Bt)
+    ldc32, ldc8 = _s8_outputs(C32, C8, M, N)
+    _vec(zA_row, "zA_row", M, torch.int32)
+    _vec(zB_col, "zB_col", N, torch.int32)
+    _vec(scale_col, "scale_col", N, torch.float32)
+    _require_cuda(A=A, Bt=Bt, C32=C32, C8=C8, zA_row=zA_row, zB_col=zB_col, scale_col=scale_col)
     rc = lib().gemm_s8_zp_noalloc(M, N, K, _ptr(A), 1 if A.dtype == torch.int8 else 0, lda,
                                   _ptr(Bt), 1 if Bt.dtype == torch.int8 else 0, ldb,
                                   int(zA), _ptr(zA_row), int(zB), _ptr(zB_col),
@@ -383,6 +403,8 @@ def gemm_s8_zp_prepare(A, Bt, workspace, M=None, N=None, K=None, stream=None):
             raise ValueError("A and Bt disagree on K")
         K = K2
         b_signed = 1 if Bt.dtype == torch.int8 else 0
+    if workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor")
     rc = lib().gemm_s8_zp_prepare(M, N, K, _ptr(A), a_signed, lda, _ptr(Bt), b_signed, ldb,
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream))
@@ -392,12 +414,19 @@ def gemm_s8_zp_prepare(A, Bt, workspace, M=None, N=None, K=None, stream=None):
 def gemm_s8_zp_run(M, N, K, a_signed, b_signed, workspace, zA=0, zA_row=None, zB=0, zB_col=None,
                    C32=None, C8=None, scale=0.0, scale_col=None, stream=None):
     """tcgen05 GEMM + fused zero-point correction / requantisation over a prepared workspace."""
-    ldc32 = C32.stride(0) if C32 is not None else 0
-    ldc8 = C8.stride(0) if C8 is not None else 0
+    import torch
+    M, N, K = int(M), int(N), int(K)
+    ldc32, ldc8 = _s8_outputs(C32, C8, M, N)
+    _vec(zA_row, "zA_row", M, torch.int32)
+    _vec(zB_col, "zB_col", N, torch.int32)
+    _vec(scale_col, "scale_col", N, torch.float32)
+    if workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor")
+    _require_cuda(C32=C32, C8=C8, zA_row=zA_row, zB_col=zB_col, scale_col=scale_col,
+                  workspace=workspace)
     rc = lib().gemm_s8_zp_run(M, N, K, int(a_signed), int(b_signed), int(zA), _ptr(zA_row),
-                              int(zB), _ptr(zB_col), _ptr(C32), max(ldc32, N if C32 is not None else 0),
-                              _ptr(C8), max(ldc8, N if C8 is not None else 0), float(scale),
-                              _ptr(scale_col), _ptr(workspace),
+                              int(zB), _ptr(zB_col), _ptr(C32), ldc32, _ptr(C8), ldc8,
+                              float(scale), _ptr(scale_col), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "gemm_s8_zp_run")
     return C32, C8

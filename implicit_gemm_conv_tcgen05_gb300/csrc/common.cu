@@ -18,9 +18,11 @@ constexpr int kMaxDevices = 64;
 __device__ unsigned long long g_status_word;
 
 std::atomic<unsigned long long> g_wait_limit{2000000000ull};
-std::atomic<int> g_tile_width{0};  // 0: chosen per problem
-std::atomic<int> g_stage_depth{0};  // 0: chosen per problem
-std::atomic<int> g_int8_path{0};    // 0: tcgen05, 1: mma.sync
+// Schedule overrides of the test hooks (igc_debug.h): per thread, so that a
+// thread that forces a schedule never changes another thread's calls.
+thread_local int t_tile_width = 0;   // 0: chosen per problem
+thread_local int t_stage_depth = 0;  // 0: chosen per problem
+thread_local int t_int8_path = 0;    // 0: tcgen05, 1: mma.sync
 std::atomic<unsigned long long> g_last_status{0};
 
 struct DeviceSlot {
@@ -120,11 +122,11 @@ unsigned long long* status_word() {
 
 unsigned long long wait_limit_ns() { return g_wait_limit.load(); }
 
-int tile_width_override() { return g_tile_width.load(); }
+int tile_width_override() { return t_tile_width; }
 
-int stage_depth_override() { return g_stage_depth.load(); }
+int stage_depth_override() { return t_stage_depth; }
 
-int int8_path_override() { return g_int8_path.load(); }
+int int8_path_override() { return t_int8_path; }
 
 int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
@@ -204,17 +206,23 @@ uint64_t igc_last_device_status(void) { return igc::g_last_status.load(); }
 
 int igc_set_tile_width(int bn) {
   if (bn != 0 && bn != 128 && bn != 224 && bn != 256) return -1;
-  return igc::g_tile_width.exchange(bn);
+  const int old = igc::t_tile_width;
+  igc::t_tile_width = bn;
+  return old;
 }
 
 int igc_set_stage_depth(int k) {
   if (k != 0 && k != 64 && k != 128) return -1;
-  return igc::g_stage_depth.exchange(k);
+  const int old = igc::t_stage_depth;
+  igc::t_stage_depth = k;
+  return old;
 }
 
 int igc_set_int8_path(int path) {
   if (path != IGC_INT8_PATH_TCGEN05 && path != IGC_INT8_PATH_MMA_SYNC) return -1;
-  return igc::g_int8_path.exchange(path);
+  const int old = igc::t_int8_path;
+  igc::t_int8_path = path;
+  return old;
 }
 
 uint64_t igc_set_wait_limit_ns(uint64_t limit_ns) {

@@ -18,6 +18,7 @@
 //     with zA'_i = zA_i - oA and zB'_j = zB_j - oB -- the zero-point expansion of
 //     sum_k (A'[i,k] - zA'_i)(B'[j,k] - zB'_j) = sum_k (A_q - zA_i)(B_q - zB_j),
 //     then C8 = clamp(rne(fp32(C32) * scale_j), -128, 127).
+#include <atomic>
 #include <mutex>
 
 #include "int8_prepass.cuh"
@@ -275,32 +276,32 @@ constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(IGC_NOALLOC_SCRATCH_
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-struct NoAllocSlot {
-  std::once_flag once;
-  void* ptr = nullptr;
-  int rc = IGC_ERR_CUDA;
-};
-NoAllocSlot g_noalloc_slots[64];
+// Device address of g_noalloc_scratch per device, cached once a lookup succeeded
+// (a failed lookup is not cached: the next call tries again).
+std::atomic<void*> g_noalloc_ptr[64];
+std::mutex g_noalloc_mutex;
 
 // Device address of g_noalloc_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// array's name is only a host-side stand-in, so the address is looked up with
+// the device current (cudaGetSymbolAddress) and cached.
 int noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return IGC_ERR_CUDA;
   if (dev < 0 || dev >= 64) return IGC_ERR_UNSUPPORTED;
-  NoAllocSlot& s = g_noalloc_slots[dev];
-  std::call_once(s.once, [&] {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) == cudaSuccess && p != nullptr) {
-      s.ptr = p;
-      s.rc = IGC_OK;
-    } else {
-      s.rc = IGC_ERR_CUDA;
+  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return IGC_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev].store(p, std::memory_order_release);
     }
-  });
-  *out = s.ptr;
-  return s.rc;
+  }
+  *out = p;
+  return IGC_OK;
 }
 
 }  // namespace
@@ -311,7 +312,19 @@ extern "C" int gemm_s8_zp_noalloc(int64_t M, int64_t N, int64_t K, const void* A
                                   const int32_t* zB_col, int32_t* C32, int64_t ldc32, int8_t* C8,
                                   int64_t ldc8, float scale, const float* scale_col,
                                   igc_stream_t stream) {
-  if (M < 0 || N < 0 || K < 0) return IGC_ERR_INVALID_ARG;
+  // the argument checks of gemm_s8_zp come first, so that a bad argument is
+  // reported as such whatever the problem's size
+  int rc0 = check_common(M, N, K);
+  if (rc0 != IGC_OK) return rc0;
+  if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
+  if (C32 == nullptr && C8 == nullptr) return IGC_ERR_INVALID_ARG;
+  if ((C32 != nullptr && ldc32 < N) || (C8 != nullptr && ldc8 < N)) return IGC_ERR_INVALID_ARG;
+  if (K == 0)  // an empty sum needs no scratch: C32 = 0, C8 = 0
+    return gemm_s8_zp(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, zA, zA_row, zB, zB_col, C32,
+                      ldc32, C8, ldc8, scale, scale_col, nullptr, 0, stream);
+  if (A == nullptr || Bt == nullptr || lda < K || ldb < K) return IGC_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Bt) || lda % 16 != 0 || ldb % 16 != 0)
+    return IGC_ERR_MISALIGNED;
   if (gemm_s8_zp_workspace_size(M, N, K) > kNoAllocScratchBytes) return IGC_ERR_WORKSPACE;
   void* scratch = nullptr;
   const int rc = noalloc_scratch(&scratch);

@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "igc.h"
+#include "igc_debug.h"
 
 namespace igc {
 
@@ -26,7 +27,8 @@ unsigned long long* status_word();
 
 // Wait limit for kernels launched now.
 unsigned long long wait_limit_ns();
-int tile_width_override();  // 0, or the tile width set by igc_set_tile_width
+// The calling thread's schedule overrides (test hooks of igc_debug.h).
+int tile_width_override();   // 0, or the tile width set by igc_set_tile_width
 int stage_depth_override();  // 0, or the stage depth set by igc_set_stage_depth
 int int8_path_override();    // 0 (tcgen05) or 1 (mma.sync), set by igc_set_int8_path
 

@@ -34,7 +34,10 @@
  *    stores.
  *  - Device: an sm_103 GPU (GB300); any other returns IGC_ERR_UNSUPPORTED.
  *  - Calls are stateless and re-entrant; concurrent calls on different streams
- *    are independent (each gemm_s8_zp call needs its own workspace).
+ *    are independent (each gemm_s8_zp call needs its own workspace).  The
+ *    schedule of a call depends only on its arguments and the device, unless
+ *    the calling thread itself forced one through the test hooks of
+ *    igc_debug.h (thread-local: they never reach another thread's calls).
  *  - Launch: kernels use programmatic dependent launch -- a kernel may start
  *    while the previous kernel in the stream finishes, and waits for it before
  *    touching memory -- so stream order is kept as with plain launches.  Calls
@@ -232,9 +235,23 @@ int gemm_s8_zp_dequant(int64_t M, int64_t N, int64_t K,
  *  - Problems whose gemm_s8_zp_workspace_size(M, N, K) exceeds
  *    IGC_NOALLOC_SCRATCH_BYTES are rejected with IGC_ERR_WORKSPACE before
  *    anything is enqueued (e.g. 2048^3 fits, 4096^3 does not).
- *  - The first call on a device looks up the device address of the scratch
- *    array (cudaGetSymbolAddress, with that device current) and caches it;
- *    make that first call before any stream capture.
+ *  - When the array is reserved: the library's int8 kernels and this array
+ *    sit in one device module, which CUDA loads on a device the first time
+ *    the process uses it there (with lazy module loading, CUDA's default):
+ *    the first call of this entry point, or any earlier gemm_s8_zp /
+ *    gemm_s8_zp_prepare / gemm_s8_zp_run / gemm_s8_zp_dequant call.  That
+ *    first use reserves the IGC_NOALLOC_SCRATCH_BYTES on the device and can
+ *    fail if the device is full.  A caller that must not allocate while
+ *    serving therefore makes one call per device at start-up, before its
+ *    memory pool claims the GPU; later calls reserve nothing more.
+ *  - The first call on a device also looks up the device address of the
+ *    scratch array (cudaGetSymbolAddress, with that device current) and
+ *    caches it once the lookup succeeds (a failed lookup returns
+ *    IGC_ERR_CUDA and is tried again on the next call); make that first call
+ *    before any stream capture.
+ *  - Arguments are checked in gemm_s8_zp's order before the size: a bad
+ *    argument returns IGC_ERR_INVALID_ARG / IGC_ERR_MISALIGNED whatever the
+ *    size, and K == 0 (all outputs zero) needs no scratch.
  *  - Every call shares the one array and leaves its contents behind; each
  *    call rewrites everything it later reads, so nothing needs clearing.
  *    Calls that overlap on the GPU (e.g. on two streams at once) race on the
@@ -336,60 +353,11 @@ uint64_t igc_last_device_status(void);
 /*
  * Limit, in nanoseconds, of every kernel-side pipeline wait launched after
  * this call (default 2e9; values < 1000 are raised to 1000).  Returns the
- * previous limit.  Process-wide.
+ * previous limit.  Process-wide: it is the one setting shared by all threads
+ * (a safety limit on how long a broken pipeline may wait, not a tuning knob;
+ * it does not change any result).
  */
 uint64_t igc_set_wait_limit_ns(uint64_t limit_ns);
-
-/*
- * Tuning and test hook: the output tile width (columns of B per CTA pair) of
- * every GEMM / convolution launched after this call.  0 (the default) picks it
- * per problem; 128, 224 or 256 force it where the operation is built for it
- * (the integer paths have 128 and 256; a width an operation lacks is ignored
- * for it).  Results do not depend on the width beyond fp32 rounding order
- * (integer results are identical).  Returns the previous setting, or -1 (and
- * changes nothing) for any other value.  Process-wide.
- */
-int igc_set_tile_width(int bn);
-
-/*
- * Tuning and test hook: the k depth of the shared-memory pipeline stages of
- * the fp16 / bf16 GEMMs and the fp16 convolution launched after this call.
- * 0 (the default) picks it per problem: 64-deep stages (twice as many, more
- * bytes in flight) for a GEMM whose schedule is at most two rounds of tiles
- * over the CTA pairs, whose tiles fill at least a quarter of them and whose
- * K >= 2048, else 128-deep (always 128 for a convolution); 64 or 128 force
- * it.  The integer paths always use 128.  Results do not depend on the depth
- * beyond fp32 rounding order.  Returns the previous setting, or -1 (and
- * changes nothing) for any other value.  Process-wide.
- */
-int igc_set_stage_depth(int k);
-
-/*
- * Selects the tensor path of gemm_s8_zp (the combined call; the prepare / run
- * split, gemm_s8_zp_dequant and the convolutions always use tcgen05) for calls
- * made after this one:
- *  IGC_INT8_PATH_TCGEN05 (default): exact integers on the tcgen05 fp16 pipe
- *    after the operand pre-pass (gemm_s8_zp above).
- *  IGC_INT8_PATH_MMA_SYNC: warp-level mma.sync m16n8k32 on the raw uint8 /
- *    int8 operands into int32 registers, raw row / column sums in the
- *    workspace's sum slots, the same correction and requantisation ([P1] §2.3's
- *    IMMA form).  Bit-identical results; far slower on sm_103a, whose
- *    warp-level integer MMA rate is a fraction of the tcgen05 fp16 rate.
- * Returns the previous setting, or -1 (and changes nothing) for any other
- * value.  Process-wide.
- */
-#define IGC_INT8_PATH_TCGEN05 0
-#define IGC_INT8_PATH_MMA_SYNC 1
-int igc_set_int8_path(int path);
-
-/*
- * Diagnostic: launches one CTA that waits on an mbarrier nothing ever
- * completes, with the current wait limit, and returns.  The wait gives up
- * after the limit and records IGC_ERR_DEVICE_TIMEOUT for
- * igc_check_device_status(); the context stays usable.  Used to test the
- * failure path without faulting or hanging the GPU.
- */
-int igc_debug_wait_timeout_probe(igc_stream_t stream);
 
 /*
  * igc_plan_gemm -- the schedule a GEMM call would run with, computed on the
@@ -406,7 +374,8 @@ int igc_debug_wait_timeout_probe(igc_stream_t stream);
  *            [3] n-tiles, [4] first column-half unit (= tiles when the last
  *            round is not split), [5] work units, [6] CTAs launched, [7] leading
  *            units per CTA pair whose operand panels are prefetched into L2.
- *  The current igc_set_tile_width / igc_set_stage_depth overrides apply.
+ *  The calling thread's igc_set_tile_width / igc_set_stage_depth overrides
+ *  (igc_debug.h) apply.
  *  Returns IGC_OK, IGC_ERR_INVALID_ARG (null out, size < 1, unknown op),
  *  IGC_ERR_UNSUPPORTED (sizes beyond 2^31 - 1) or a device error when clusters
  *  <= 0 and no usable device is present.

@@ -13,7 +13,7 @@ import implicit_gemm_conv_tcgen05_gb300 as igc
 
 def test_library_loads_and_exports_every_declared_symbol():
     L = igc.lib()
-    names = igc.declared_functions()
+    names = igc.declared_functions(igc.HEADER) + igc.declared_functions(igc.DEBUG_HEADER)
     expected = {"gemm_f16", "gemm_bf16", "gemm_s8_zp", "gemm_s8_zp_workspace_size", "gemm_s8_zp_prepare",
                 "gemm_s8_zp_run", "gemm_s8_zp_dequant", "gemm_s8_zp_noalloc",
                 "conv2d_nhwc_s8_zp", "conv2d_nhwc_s8_zp_workspace_size", "conv2d_nhwc_f16_implicit",
@@ -134,7 +134,7 @@ def test_header_is_c99_and_links_from_c(tmp_path):
     lib = igc.lib()._name
     src = tmp_path / "use_igc.c"
     src.write_text(
-        '#include <string.h>\n#include "igc.h"\n'
+        '#include <string.h>\n#include "igc.h"\n#include "igc_debug.h"\n'
         "int main(void) {\n"
         "  int32_t out[8];\n"
         "  if (igc_plan_gemm(IGC_PLAN_GEMM_F16, 4096, 4096, 4096, 76, out) != IGC_OK) return 1;\n"
@@ -148,3 +148,90 @@ def test_header_is_c99_and_links_from_c(tmp_path):
     subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), lib, "-o", str(exe),
                     f"-Wl,-rpath,{os.path.dirname(lib)}"], check=True)
     assert subprocess.run([str(exe)]).returncode == 0
+
+
+def test_headers_declare_exactly_the_boundary_and_the_debug_hooks():
+    """include/igc.h holds the operations of the path and their documented
+    companions only; the schedule-forcing test hooks live in include/igc_debug.h."""
+    product = {"gemm_f16", "gemm_bf16", "gemm_s8_zp", "gemm_s8_zp_workspace_size",
+               "gemm_s8_zp_prepare", "gemm_s8_zp_run", "gemm_s8_zp_dequant",
+               "gemm_s8_zp_noalloc", "conv2d_nhwc_f16_implicit", "conv2d_nhwc_s8_zp",
+               "conv2d_nhwc_s8_zp_workspace_size", "igc_status_string",
+               "igc_check_device_status", "igc_last_device_status", "igc_set_wait_limit_ns",
+               "igc_plan_gemm", "igc_version"}
+    debug = {"igc_set_tile_width", "igc_set_stage_depth", "igc_set_int8_path",
+             "igc_debug_wait_timeout_probe"}
+    assert set(igc.declared_functions(igc.HEADER)) == product
+    assert set(igc.declared_functions(igc.DEBUG_HEADER)) == debug
+    L = igc.lib()
+    for n in product | debug:
+        assert ctypes.cast(getattr(L, n), ctypes.c_void_p).value, n
+
+
+def test_schedule_hooks_are_thread_local():
+    """A hook set on one thread is invisible to calls made on another thread."""
+    import threading
+    seen = {}
+
+    def other():
+        # a fresh thread starts at the defaults and its settings stay its own
+        seen["width"] = igc.igc_set_tile_width(128)
+        seen["depth"] = igc.igc_set_stage_depth(64)
+        seen["path"] = igc.igc_set_int8_path(igc.INT8_PATH_MMA_SYNC)
+        seen["plan"] = igc.igc_plan_gemm(igc.PLAN_GEMM_F16, 4096, 4096, 4096, clusters=76)
+
+    assert igc.igc_set_tile_width(224) == 0
+    assert igc.igc_set_stage_depth(128) == 0
+    assert igc.igc_set_int8_path(igc.INT8_PATH_TCGEN05) == 0
+    try:
+        th = threading.Thread(target=other)
+        th.start()
+        th.join()
+        assert seen["width"] == 0 and seen["depth"] == 0 and seen["path"] == 0
+        assert seen["plan"]["tile_width"] == 128 and seen["plan"]["stage_k"] == 64
+        # this thread's settings were not touched by the other thread
+        plan = igc.igc_plan_gemm(igc.PLAN_GEMM_F16, 4096, 4096, 4096, clusters=76)
+        assert plan["tile_width"] == 224 and plan["stage_k"] == 128
+        assert igc.igc_set_tile_width(0) == 224
+        assert igc.igc_set_stage_depth(0) == 128
+    finally:
+        igc.igc_set_tile_width(0)
+        igc.igc_set_stage_depth(0)
+        igc.igc_set_int8_path(igc.INT8_PATH_TCGEN05)
+
+
+def test_binding_checks_outputs_and_vectors_before_the_device():
+    """Short or mistyped outputs and vectors raise on the host: the C entry points
+    take raw pointers and cannot see a buffer's length."""
+    import torch
+    A = torch.zeros((64, 32), dtype=torch.uint8)
+    Bt = torch.zeros((48, 32), dtype=torch.int8)
+    ws = torch.zeros(igc.gemm_s8_zp_workspace_size(64, 48, 32), dtype=torch.uint8)
+    C8 = torch.zeros((64, 48), dtype=torch.int8)
+    short8 = torch.zeros((63, 48), dtype=torch.int8)
+    short32 = torch.zeros((64, 47), dtype=torch.int32)
+    with pytest.raises(ValueError, match="C8 has shape"):
+        igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C8=short8, scale=1.0)
+    with pytest.raises(ValueError, match="C32 has shape"):
+        igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C32=short32)
+    with pytest.raises(TypeError, match="C8 has dtype"):
+        igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C8=C8.view(torch.uint8), scale=1.0)
+    with pytest.raises(ValueError, match="scale_col must be"):
+        igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C8=C8, scale_col=torch.ones(47))
+    with pytest.raises(ValueError, match="zA_row must be"):
+        igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C8=C8, scale=1.0,
+                           zA_row=torch.zeros(64, dtype=torch.int64))
+    with pytest.raises(ValueError, match="zB_col must be"):
+        igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C8=C8, scale=1.0,
+                           zB_col=torch.zeros(49, dtype=torch.int32))
+    # the same checks on the no-allocation entry point and the combined call
+    for fn in (igc.gemm_s8_zp_noalloc, igc.gemm_s8_zp):
+        with pytest.raises(ValueError, match="C8 has shape"):
+            fn(A, Bt, C8=short8, scale=1.0)
+        with pytest.raises(ValueError, match="scale_col must be"):
+            fn(A, Bt, C8=C8, scale_col=torch.ones(50))
+    # right shapes and dtypes, host memory: rejected as not being CUDA tensors
+    with pytest.raises(ValueError, match="CUDA"):
+        igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C8=C8, scale=1.0)
+    with pytest.raises(ValueError, match="Y has shape"):
+        igc.gemm_s8_zp_dequant(A, Bt, Y=torch.zeros((64, 47), dtype=torch.float32))

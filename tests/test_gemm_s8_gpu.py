@@ -207,3 +207,40 @@ def test_outputs_at_unaligned_addresses_use_direct_stores():
     _assert_equal(g8[:, 1:1 + N], o8, "C8")
     assert np.all(g32[:, 0] == 9) and np.all(g32[:, 1 + N:] == 9)
     assert np.all(g8[:, 0] == 9) and np.all(g8[:, 1 + N:] == 9)
+
+
+def test_running_sum_near_2_pow_24_with_unit_products_in_one_mma():
+    """A 1024-k chunk whose running sum reaches 2^24 - 16384 before its last 16-k
+    MMA, which mixes (-128)(-128) products with +-1 and +-128 products (so the
+    chunk ends at 2^24 - 16384 +- 1, an odd integer at the top exponent); the
+    next chunk does the same with 127 x (-128) products and its unit products in
+    the middle.  Every C32 must be exact (uint8 A with zA = 128 gives the shifted
+    operand A - 128; int8 B with zB = 0 is used as is)."""
+    M, N, K = 256, 256, 2048
+    a = np.full((M, K), -128, np.int64)       # the shifted A values a' = A - 128
+    b = np.full((N, K), -128, np.int64)       # B values (int8, zB = 0)
+    a[:, 1024:] = 127
+    i = np.arange(M)
+    j = np.arange(N)
+    sign = np.where((i // 16) % 2 == 0, 1, -1)
+    # chunk 0: the last MMA (k 1008..1023) holds one unit entry per row and column
+    a[i, 1008 + i % 16] = sign
+    b[j, 1008 + j % 16] = 1
+    # chunk 1: unit entries in an MMA in the middle of the chunk (k 1536..1551)
+    a[i, 1536 + (i * 7) % 16] = -sign
+    b[j, 1536 + (j * 7) % 16] = -1
+    A = (a + 128).astype(np.uint8)
+    Bt = b.astype(np.int8)
+    want = a @ b.T                            # exact int64
+    assert np.abs(want).max() < 2 ** 31
+    kw = dict(zA=128, zB=0, scale=2.0 ** -20)
+    g32, g8 = _gpu(A, Bt, **kw)
+    o32, o8, ovf = _oracle(A, Bt, **kw)
+    assert not ovf
+    _assert_equal(o32, want, "oracle C32 vs int64 matmul")
+    _assert_equal(g32, want, "C32")
+    _assert_equal(g8, o8, "C8")
+    # the chunk-0 partial sums of the diagonal blocks are 2^24 - 16384 +- 1
+    part = a[:, :1024] @ b[:, :1024].T
+    diag = (i[:, None] % 16) == (j[None, :] % 16)
+    assert set(np.unique(part[diag])) == {2 ** 24 - 16384 - 1, 2 ** 24 - 16384 + 1}
