@@ -302,7 +302,10 @@ def e2e_measure(steps_objs, w3, w4, w5, steps: int, pipelined: bool):
 
 def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
     """Rows beyond the step (not part of `value`): each timed alone with CUDA events,
-    L2 flushed before every iteration, median of `iters`."""
+    L2 flushed before every iteration, median of `iters`.  After the flush a spin
+    kernel (about 100 us) keeps the GPU busy while the host enqueues the timed call,
+    so that the events bracket device time only (the call's host-side cost, about
+    10 us through the Python binding, is in the e2e figure, not in these rows)."""
     import torch
     import implicit_gemm_conv_tcgen05_gb300 as igc
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
@@ -314,6 +317,7 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
         ts = []
         for _ in range(iters):
             flush.zero_()
+            torch.cuda._sleep(200_000)
             s.record()
             fn()
             e.record()
@@ -595,7 +599,8 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_extras:
         result["extras"] = extras_measure(device, peak_burst, hbm)
-        result["extras_note"] = ("rows beyond the step, each timed alone (L2 flushed, median of "
+        result["extras_note"] = ("rows beyond the step, each timed alone on the device (L2 "
+                                 "flushed, host enqueue hidden behind a spin kernel, median of "
                                  "10; *_graph100 rows: per-call time of 100 launches replayed "
                                  "from a CUDA graph, L2 warm); not part of value")
 

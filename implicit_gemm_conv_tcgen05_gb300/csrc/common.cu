@@ -22,7 +22,7 @@ std::atomic<unsigned long long> g_wait_limit{2000000000ull};
 // thread that forces a schedule never changes another thread's calls.
 thread_local int t_tile_width = 0;   // 0: chosen per problem
 thread_local int t_stage_depth = 0;  // 0: chosen per problem
-thread_local int t_int8_path = 0;    // 0: tcgen05, 1: mma.sync
+thread_local int t_int8_path = 0;    // IGC_INT8_PATH_*
 std::atomic<unsigned long long> g_last_status{0};
 
 struct DeviceSlot {
@@ -131,6 +131,58 @@ int int8_path_override() { return t_int8_path; }
 int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                     uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                     uint32_t box_rows) {
+  return encode_tiled_2d_swizzle(map, dtype, base, inner, rows, row_stride_bytes, box_inner,
+                                 box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+namespace {
+
+// Tensor maps are pure functions of their arguments (address, extents, stride,
+// box, swizzle), so the ones a thread encoded recently are kept and reused:
+// repeated calls on the same buffers skip the driver's encode.  Direct-mapped,
+// per thread (no locking); a slot holds the full key it was encoded from.
+struct TiledKey {
+  uint64_t base, inner, rows, stride;
+  uint32_t box_inner, box_rows, dtype, swizzle;
+  bool operator==(const TiledKey& o) const {
+    return base == o.base && inner == o.inner && rows == o.rows && stride == o.stride &&
+           box_inner == o.box_inner && box_rows == o.box_rows && dtype == o.dtype &&
+           swizzle == o.swizzle;
+  }
+};
+
+struct TiledSlot {
+  TiledKey key;
+  CUtensorMap map;
+  bool valid = false;
+};
+
+constexpr int kMapCacheSlots = 64;
+thread_local TiledSlot t_map_cache[kMapCacheSlots];
+
+int map_cache_index(const TiledKey& k) {
+  uint64_t h = k.base * 0x9E3779B97F4A7C15ull;
+  h ^= (k.inner + 0x632BE59BD9B4E019ull) * 0xC2B2AE3D27D4EB4Full;
+  h ^= (k.rows + (k.stride << 20)) * 0x165667B19E3779F9ull;
+  h ^= (static_cast<uint64_t>(k.box_inner) << 32 | k.box_rows) * 0x27D4EB2F165667C5ull;
+  h ^= (static_cast<uint64_t>(k.dtype) << 8 | k.swizzle) * 0x94D049BB133111EBull;
+  h ^= h >> 29;
+  return static_cast<int>(h % kMapCacheSlots);
+}
+
+}  // namespace
+
+int encode_tiled_2d_swizzle(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                            uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                            uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  const TiledKey key{reinterpret_cast<uint64_t>(base), inner, rows, row_stride_bytes,
+                     box_inner, box_rows, static_cast<uint32_t>(dtype),
+                     static_cast<uint32_t>(swizzle)};
+  TiledSlot& slot = t_map_cache[map_cache_index(key)];
+  if (slot.valid && slot.key == key) {
+    *map = slot.map;
+    return IGC_OK;
+  }
   load_encoders();
   if (!g_encode_tiled) return IGC_ERR_CUDA;
   cuuint64_t dims[2] = {inner, rows};
@@ -138,10 +190,14 @@ int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode_tiled(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? IGC_OK : IGC_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return IGC_ERR_CUDA;
+  slot.key = key;
+  slot.map = *map;
+  slot.valid = true;
+  return IGC_OK;
 }
 
 int encode_im2col_nhwc(CUtensorMap* map, const void* base, int N, int H, int W, int C,
@@ -219,7 +275,9 @@ int igc_set_stage_depth(int k) {
 }
 
 int igc_set_int8_path(int path) {
-  if (path != IGC_INT8_PATH_TCGEN05 && path != IGC_INT8_PATH_MMA_SYNC) return -1;
+  if (path != IGC_INT8_PATH_TCGEN05 && path != IGC_INT8_PATH_MMA_SYNC &&
+      path != IGC_INT8_PATH_FUSED)
+    return -1;
   const int old = igc::t_int8_path;
   igc::t_int8_path = path;
   return old;

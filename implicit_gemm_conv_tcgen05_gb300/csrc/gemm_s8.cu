@@ -21,6 +21,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "gemm_i8.cuh"
 #include "int8_prepass.cuh"
 #include "launch.cuh"
 
@@ -186,6 +187,186 @@ int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, in
   return launch_auto_bn<Mode::GemmInt>(dev, tmA, ws + l.b_off, Kp, N, Kp * 2, om, p, stream);
 }
 
+// ---------------------------------------------------------------------------
+// The fused path: int8 operands converted inside the GEMM kernel (gemm_i8.cuh)
+// ---------------------------------------------------------------------------
+template <int BN, bool kDequant>
+struct I8Slot {
+  std::once_flag once[64];
+  int rc[64];
+  int max_clusters[64];
+};
+
+template <int BN, bool kDequant>
+I8Slot<BN, kDequant>& i8_slot() {
+  static I8Slot<BN, kDequant> s;
+  return s;
+}
+
+// Shared-memory attribute and the CTA pairs that fit at once (cached per device).
+template <int BN, bool kDequant>
+int i8_setup(const DeviceInfo& dev, int* max_clusters) {
+  using Cfg = I8Cfg<BN>;
+  auto& s = i8_slot<BN, kDequant>();
+  const int d = dev.device;
+  std::call_once(s.once[d], [&] {
+    s.rc[d] = IGC_ERR_CUDA;
+    s.max_clusters[d] = 0;
+    if (dev.smem_optin < Cfg::kSmemBytes) {
+      s.rc[d] = IGC_ERR_UNSUPPORTED;
+      return;
+    }
+    auto kern = igc_i8_gemm_kernel<BN, kDequant>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Cfg::kSmemBytes)) != cudaSuccess)
+      return;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return;
+    if (fa.numRegs < kI8LaunchRegs) {  // the register split assumes 128 per thread at launch
+      s.rc[d] = IGC_ERR_UNSUPPORTED;
+      return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+    cfg.blockDim = dim3(kI8Threads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = dev.sm_count / 2;
+    }
+    s.max_clusters[d] = n;
+    s.rc[d] = IGC_OK;
+  });
+  *max_clusters = s.max_clusters[d];
+  return s.rc[d];
+}
+
+template <int BN, bool kDequant>
+int launch_i8(const DeviceInfo& dev, const CUtensorMap& tmA, const void* Bt, int64_t N,
+              int64_t K, int64_t ldb, const OutMaps& om, KParams p, uint32_t flipA,
+              uint32_t flipB, int clusters_avail, cudaStream_t stream) {
+  CUtensorMap tmB, tmBh;
+  int rc = encode_tiled_2d_swizzle(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bt,
+                                   static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                                   static_cast<uint64_t>(ldb), kI8KS, BN / 2,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != IGC_OK) return rc;
+  rc = encode_tiled_2d_swizzle(&tmBh, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bt,
+                               static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                               static_cast<uint64_t>(ldb), kI8KS, BN / 4,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != IGC_OK) return rc;
+  int max_clusters = 0;
+  rc = i8_setup<BN, kDequant>(dev, &max_clusters);
+  if (rc != IGC_OK) return rc;
+  (void)clusters_avail;
+  p.tiles_m = static_cast<int>((static_cast<long long>(p.M) + BM - 1) / BM);
+  p.tiles_n = static_cast<int>((static_cast<long long>(p.N) + BN - 1) / BN);
+  const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fff0000LL) return IGC_ERR_UNSUPPORTED;
+  p.num_tiles = static_cast<int>(tiles);
+  p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;
+  p.tail_start = tail_start_of(p.num_tiles, max_clusters);
+  p.num_units = p.num_tiles + (p.num_tiles - p.tail_start);
+  p.wait_limit_ns = wait_limit_ns();
+  p.status = status_word();
+  p.tma_out = om.mask;
+  const int clusters = p.num_units < max_clusters ? p.num_units : max_clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kI8Threads, 1, 1);
+  cfg.dynamicSmemBytes = I8Cfg<BN>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, igc_i8_gemm_kernel<BN, kDequant>, tmA, tmB, tmBh, om.map[0], om.map[1],
+                         om.map[2], p, flipA, flipB) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return IGC_ERR_CUDA;
+  }
+  return IGC_OK;
+}
+
+// gemm_s8_zp / gemm_s8_zp_dequant on the fused path: arguments as for
+// run_int_gemm plus the raw operands (K >= 1, checked by the caller's rules).
+int run_int_gemm_fused(int64_t M, int64_t N, int64_t K, const void* A, int a_signed, int64_t lda,
+                       const void* Bt, int b_signed, int64_t ldb, int32_t zA,
+                       const int32_t* zA_row, int32_t zB, const int32_t* zB_col, int32_t* C32,
+                       int64_t ldc32, int8_t* C8, int64_t ldc8, float scale,
+                       const float* scale_col, const DequantOut& dq, cudaStream_t stream) {
+  if (A == nullptr || Bt == nullptr || lda < K || ldb < K) return IGC_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Bt) || lda % 16 != 0 || ldb % 16 != 0)
+    return IGC_ERR_MISALIGNED;
+  DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc != IGC_OK) return rc;
+  CUtensorMap tmA;
+  rc = encode_tiled_2d_swizzle(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, static_cast<uint64_t>(K),
+                               static_cast<uint64_t>(M), static_cast<uint64_t>(lda), kI8KS,
+                               BM_CTA, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != IGC_OK) return rc;
+  KParams p{};
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.num_kb = static_cast<int>((K + kI8KS - 1) / kI8KS);
+  p.chunk_kb = kI8ChunkKb;
+  p.c32 = C32;
+  p.ldc32 = ldc32;
+  p.c8 = C8;
+  p.ldc8 = ldc8;
+  p.zA = zA;
+  p.zA_row = zA_row;
+  p.zB = zB;
+  p.zB_col = zB_col;
+  p.oA = a_signed ? 0 : 128;
+  p.oB = b_signed ? 0 : 128;
+  p.scale = scale;
+  p.scale_col = scale_col;
+  p.yf = dq.y;
+  p.ldyf = dq.ldy;
+  p.dq_row = dq.dq_row;
+  p.dq_col = dq.dq_col;
+  p.bias = dq.bias;
+  p.vec_ok = vec_store_ok(C32, ldc32, 4) && vec_store_ok(C8, ldc8, 1) &&
+             vec_store_ok(dq.y, dq.ldy, 4);
+  OutMaps om;
+  add_out_map(om, 0, CU_TENSOR_MAP_DATA_TYPE_INT32, C32, ldc32, M, N, 4);
+  add_out_map(om, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, C8, ldc8, M, N, 1);
+  add_out_map(om, 2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dq.y, dq.ldy, M, N, 4);
+  // uint8 keeps its byte (u = value + 128 - 128 offset), int8 flips the top bit
+  const uint32_t flipA = a_signed ? 0x80808080u : 0u;
+  const uint32_t flipB = b_signed ? 0x80808080u : 0u;
+  int clusters = 0;
+  rc = i8_setup<256, false>(dev, &clusters);
+  if (rc != IGC_OK) return rc;
+  int bn = pick_bn(M, N, clusters, kBnCandsInt, kBnEffInt, 2);
+  bn = apply_width_override(bn, true);
+  const bool dq_out = dq.y != nullptr;
+  if (bn == 128)
+    return dq_out ? launch_i8<128, true>(dev, tmA, Bt, N, K, ldb, om, p, flipA, flipB, clusters,
+                                         stream)
+                  : launch_i8<128, false>(dev, tmA, Bt, N, K, ldb, om, p, flipA, flipB, clusters,
+                                          stream);
+  return dq_out ? launch_i8<256, true>(dev, tmA, Bt, N, K, ldb, om, p, flipA, flipB, clusters,
+                                       stream)
+                : launch_i8<256, false>(dev, tmA, Bt, N, K, ldb, om, p, flipA, flipB, clusters,
+                                        stream);
+}
+
 }  // namespace
 
 extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
@@ -212,15 +393,19 @@ extern "C" int gemm_s8_zp_dequant(int64_t M, int64_t N, int64_t K, const void* A
   if (Y == nullptr || ldy < N) return IGC_ERR_INVALID_ARG;
   if (K == 0) return IGC_ERR_UNSUPPORTED;
   if (A == nullptr || Bt == nullptr) return IGC_ERR_INVALID_ARG;
-  rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,
-                          workspace_bytes, stream);
-  if (rc != IGC_OK) return rc;
   DequantOut dq;
   dq.y = Y;
   dq.ldy = ldy;
   dq.dq_row = scale_row;
   dq.dq_col = scale_col;
   dq.bias = bias;
+  if (int8_path_override() == IGC_INT8_PATH_FUSED)
+    return run_int_gemm_fused(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, zA, zA_row, zB,
+                              zB_col, nullptr, 0, nullptr, 0, 0.0f, nullptr, dq,
+                              reinterpret_cast<cudaStream_t>(stream));
+  rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,
+                          workspace_bytes, stream);
+  if (rc != IGC_OK) return rc;
   return run_int_gemm(M, N, K, a_signed, b_signed, zA, zA_row, zB, zB_col, nullptr, 0, nullptr,
                       0, 0.0f, nullptr, dq, workspace, workspace_bytes,
                       reinterpret_cast<cudaStream_t>(stream));
@@ -254,6 +439,10 @@ extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_
                            reinterpret_cast<int32_t*>(ws + l.cb_off),
                            reinterpret_cast<cudaStream_t>(stream));
   }
+  if (K > 0 && int8_path_override() == IGC_INT8_PATH_FUSED)
+    return run_int_gemm_fused(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, zA, zA_row, zB,
+                              zB_col, C32, ldc32, C8, ldc8, scale, scale_col, DequantOut(),
+                              reinterpret_cast<cudaStream_t>(stream));
   if (K > 0) {
     if (A == nullptr || Bt == nullptr) return IGC_ERR_INVALID_ARG;
     rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,

@@ -88,6 +88,8 @@ constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 216;
 constexpr int kMinLaunchRegs = 168;
 static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kThreads * kMinLaunchRegs, "register split");
+// setmaxnreg.dec only lowers and setmaxnreg.inc only raises a warpgroup's count
+static_assert(kRegsLow <= kMinLaunchRegs && kRegsHigh >= kMinLaunchRegs, "register split direction");
 constexpr uint32_t kAtomABytes = BM_CTA * BK * 2;   // 16 KB
 constexpr uint32_t kBarrierBytes = 512;
 // Each epilogue warp stages 32 rows x 128 bytes of output in shared memory (128-byte
@@ -666,10 +668,19 @@ struct IntRow {
   float sA;            // dequantisation row scale
 };
 
-__device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
+// The row terms from rs = rA'_i, the row sum of the shifted A operand.
+__device__ __forceinline__ IntRow int_row_from(const KParams& p, int m, uint32_t rs) {
   const int mm = m < p.M ? m : p.M - 1;  // rows past M are computed (and clipped) like row M-1
   IntRow r;
   r.zAp = static_cast<uint32_t>((p.zA_row ? __ldg(p.zA_row + mm) : p.zA) - p.oA);
+  r.u = rs - static_cast<uint32_t>(p.K) * r.zAp;
+  r.t_uniform = static_cast<uint32_t>(p.zB - p.oB) * r.u;
+  r.sA = p.dq_row ? __ldg(p.dq_row + mm) : 1.0f;
+  return r;
+}
+
+__device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
+  const int mm = m < p.M ? m : p.M - 1;  // rows past M are computed (and clipped) like row M-1
   uint32_t rs;
   if (p.px != nullptr) {
     const int PQ = p.conv_P * p.conv_Q;
@@ -686,10 +697,7 @@ __device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
   } else {
     rs = static_cast<uint32_t>(__ldg(p.rsumA + mm));
   }
-  r.u = rs - static_cast<uint32_t>(p.K) * r.zAp;
-  r.t_uniform = static_cast<uint32_t>(p.zB - p.oB) * r.u;
-  r.sA = p.dq_row ? __ldg(p.dq_row + mm) : 1.0f;
-  return r;
+  return int_row_from(p, m, rs);
 }
 
 // C32 of the kG columns of group j (tile columns j kG ...).
@@ -745,14 +753,17 @@ __device__ __forceinline__ void float_group(const KParams& p, const IntRow& r,
 // of the warp must call it and run every group: the column values are broadcast
 // by shuffles and the TMA paths are warp-collective; only the direct stores are
 // predicated on the row.
-template <int NC>
-__device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMap& tmO0,
-                                              const CUtensorMap& tmO1, const CUtensorMap& tmO2,
-                                              const Stager& st, int m, int n0,
-                                              const uint32_t (&sum)[NC]) {
-  const IntRow r = int_row(p, m);
-  ColVecs<NC> V;
-  load_col_vecs<NC>(p, n0, st.lane, V);
+// store_row_int_v takes the row terms and the column vectors ready-made (the
+// kernel that converts its operands itself takes the sums from shared memory);
+// store_row_int reads them from global memory.
+// kDequant false: the caller guarantees p.yf == nullptr (no dequantised output),
+// which drops that output's code and registers.
+template <int NC, bool kDequant = true>
+__device__ __forceinline__ void store_row_int_v(const KParams& p, const CUtensorMap& tmO0,
+                                                const CUtensorMap& tmO1, const CUtensorMap& tmO2,
+                                                const Stager& st, int m, int n0,
+                                                const uint32_t (&sum)[NC], const IntRow& r,
+                                                const ColVecs<NC>& V) {
   const bool in_row = m < p.M;
   const bool full = p.vec_ok && (n0 + NC <= p.N);
   // int8 (requantised)
@@ -799,7 +810,7 @@ __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMa
   // int32 and dequantised fp32: 32-bit values, boxes of 32 columns (two groups);
   // one copy of the loop body for both outputs keeps the register count down
 #pragma unroll 1
-  for (int o = 0; o < 2; ++o) {
+  for (int o = 0; o < (kDequant ? 2 : 1); ++o) {
     void* outp = o == 0 ? static_cast<void*>(p.c32) : static_cast<void*>(p.yf);
     if (outp == nullptr) continue;
     const bool tma = (p.tma_out >> (o == 0 ? 0 : 2)) & 1;
@@ -815,7 +826,7 @@ __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMa
         int32_t c[kG];
         uint32_t y[kG];
         int_group<NC>(p, r, V, sum, j, c);
-        if (o == 0) {
+        if (!kDequant || o == 0) {
 #pragma unroll
           for (int i = 0; i < kG; ++i) y[i] = static_cast<uint32_t>(c[i]);
         } else {
@@ -841,6 +852,17 @@ __device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMa
       if (tma) st.issue(map, n0 + b * 32);
     }
   }
+}
+
+template <int NC>
+__device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMap& tmO0,
+                                              const CUtensorMap& tmO1, const CUtensorMap& tmO2,
+                                              const Stager& st, int m, int n0,
+                                              const uint32_t (&sum)[NC]) {
+  const IntRow r = int_row(p, m);
+  ColVecs<NC> V;
+  load_col_vecs<NC>(p, n0, st.lane, V);
+  store_row_int_v<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum, r, V);
 }
 
 // Loads NC consecutive TMEM columns (this warp's 32 lanes) into v: 32 columns
@@ -886,6 +908,24 @@ __device__ __forceinline__ void tmem_drain(uint32_t taddr, uint32_t (&sum)[NC], 
         sum[j * 64 + i] += static_cast<uint32_t>(__float2int_rz(__uint_as_float(r0[i])));
         sum[j * 64 + 32 + i] += static_cast<uint32_t>(__float2int_rz(__uint_as_float(r1[i])));
       }
+    }
+  }
+}
+
+// tmem_drain with one 32-column load per wait (half the registers in flight),
+// for epilogues that run with a smaller register budget.
+template <int NC>
+__device__ __forceinline__ void tmem_drain_x32(uint32_t taddr, uint32_t (&sum)[NC], bool first) {
+  static_assert(NC % 32 == 0, "drain in steps of 32 columns");
+#pragma unroll
+  for (int j = 0; j < NC / 32; ++j) {
+    uint32_t r0[32];
+    tmem_ld_32x32b_x32(taddr + j * 32, r0);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t v = static_cast<uint32_t>(__float2int_rz(__uint_as_float(r0[i])));
+      sum[j * 32 + i] = first ? v : sum[j * 32 + i] + v;
     }
   }
 }
@@ -986,10 +1026,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
-  // Set-up above touches no global memory; from here on the previous kernel in
-  // the stream must have finished (programmatic dependent launch).
-  grid_dependency_wait();
-  grid_dependents_launch();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
   // The pair's MMAs write both CTAs' tensor memory at the leader's address: both

@@ -45,28 +45,29 @@ int encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                     uint64_t inner, uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                     uint32_t box_rows);
 
+// The same with a chosen swizzle (encode_tiled_2d: 128-byte).
+int encode_tiled_2d_swizzle(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                            uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                            uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
 int encode_im2col_nhwc(CUtensorMap* map, const void* base, int N, int H, int W, int C,
                        int lower_h, int lower_w, int upper_h, int upper_w, uint32_t channels,
                        uint32_t pixels, int stride_h, int stride_w);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Launches a non-cluster kernel with programmatic stream serialization: it may
-// start while the previous kernel in the stream runs and waits for it in the
-// kernel (griddepcontrol.wait) before touching memory.
+// Launches a non-cluster kernel on `stream` (cudaLaunchKernelEx, no launch
+// attributes); returns IGC_OK or IGC_ERR_CUDA.
 template <typename... Params, typename... Args>
-int launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-               Args&&... args) {
+int launch_plain(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                 cudaStream_t stream, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
   if (cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...) != cudaSuccess) {
     (void)cudaGetLastError();
     return IGC_ERR_CUDA;

@@ -73,6 +73,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with acquire semantics at cluster scope: the phase may have been
+// completed by arrivals (release.cluster) from threads of the peer CTA.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t clock_cycles() {
   uint64_t c;
   asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
@@ -86,19 +100,24 @@ __device__ __forceinline__ uint64_t clock_cycles() {
 // completes or a short hardware window passes); the limit is kept with the
 // SM cycle counter, read once per 64 tries, at 2 cycles per nanosecond (the
 // SM clock is at most 2.1 GHz, so the limit is never shorter than asked).
+// kCluster: acquire at cluster scope (for phases completed from the peer CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int* abort, unsigned long long* status,
                                           uint32_t site) {
   const uint32_t addr = smem_u32(bar);
+  auto try_once = [&]() {
+    return kCluster ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity);
+  };
 #pragma unroll 1
   for (int i = 0; i < 64; ++i)
-    if (mbar_try_wait(addr, parity)) return true;
+    if (try_once()) return true;
   const uint64_t c0 = clock_cycles();
   const uint64_t limit_cycles = 2ull * limit_ns;
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
+      if (try_once()) return true;
     if (*abort) return false;
     if (clock_cycles() - c0 > limit_cycles) {
       *abort = 1;
@@ -106,20 +125,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
       return false;
     }
   }
-}
-
-// ---------------------------------------------------------------------------
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialization may start while the previous kernel in the stream is still
-// running; it must wait here before touching memory that kernel writes or
-// reads.  The trigger lets the next kernel start its own set-up early.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void grid_dependents_launch() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -249,6 +254,31 @@ __device__ __forceinline__ void cluster_sync() {
 // already ordered by tcgen05.wait::ld and tcgen05.fence::before_thread_sync.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Arrive on an mbarrier given by its cluster address (this CTA's or the peer's)
+// with release semantics at cluster scope: memory accesses ordered before the
+// arrival are visible to a thread that acquires the phase at cluster scope
+// (mbar_wait<true>), whichever CTA it runs in.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Arrive on a barrier of this CTA (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 2-D tiled TMA load into this CTA's shared memory, completion on this CTA's
+// barrier `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
 }
 
 // TMA loads into this CTA's shared memory whose completion is signalled on an

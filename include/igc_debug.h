@@ -46,22 +46,31 @@ int igc_set_tile_width(int bn);
 int igc_set_stage_depth(int k);
 
 /*
- * Selects the tensor path of gemm_s8_zp (the combined call; the prepare / run
- * split, gemm_s8_zp_dequant and the convolutions always use tcgen05) for calls
- * made after this one:
+ * Selects the tensor path of gemm_s8_zp and gemm_s8_zp_dequant (the
+ * prepare / run split and the convolutions always take the pre-pass form)
+ * for calls made after this one:
  *  IGC_INT8_PATH_TCGEN05 (default): exact integers on the tcgen05 fp16 pipe
- *    after the operand pre-pass (gemm_s8_zp above).
- *  IGC_INT8_PATH_MMA_SYNC: warp-level mma.sync m16n8k32 on the raw uint8 /
- *    int8 operands into int32 registers, raw row / column sums in the
- *    workspace's sum slots, the same correction and requantisation ([P1] §2.3's
- *    IMMA form).  Bit-identical results; far slower on sm_103a, whose
- *    warp-level integer MMA rate is a fraction of the tcgen05 fp16 rate.
- * Returns the previous setting, or -1 (and changes nothing) for any other
- * value.  Thread-local: it applies to the calls
- * of the thread that set it and to no other thread's.
+ *    after a pre-pass kernel that writes the operands shifted to [-128, 127]
+ *    as fp16, with their row / column sums, into the workspace
+ *    (gemm_s8_zp_prepare, then gemm_s8_zp_run).
+ *  IGC_INT8_PATH_MMA_SYNC (gemm_s8_zp only; gemm_s8_zp_dequant takes the
+ *    default): warp-level mma.sync m16n8k32 on the raw uint8 / int8 operands
+ *    into int32 registers, raw row / column sums in the workspace's sum slots,
+ *    the same correction and requantisation ([P1] §2.3's IMMA form).  Far
+ *    slower on sm_103a, whose warp-level integer MMA rate is a fraction of the
+ *    tcgen05 fp16 rate.
+ *  IGC_INT8_PATH_FUSED: the same tcgen05 arithmetic with the shift and fp16
+ *    widening done inside the GEMM kernel (int8 tiles by TMA, converter warps
+ *    writing the fp16 operand stages, row / column sums in the same pass): no
+ *    pre-pass and no workspace traffic, but about 1.8x the default's time at
+ *    8192^3 on GB300, since every output tile converts its own operand panels.
+ * Every path gives bit-identical results.  Returns the previous setting, or
+ * -1 (and changes nothing) for any other value.  Thread-local: it applies to
+ * the calls of the thread that set it and to no other thread's.
  */
 #define IGC_INT8_PATH_TCGEN05 0
 #define IGC_INT8_PATH_MMA_SYNC 1
+#define IGC_INT8_PATH_FUSED 2
 int igc_set_int8_path(int path);
 
 /*

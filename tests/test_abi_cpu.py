@@ -112,8 +112,9 @@ def test_tile_width_setter_roundtrip():
 
 def test_int8_path_setter_roundtrip():
     assert igc.igc_set_int8_path(igc.INT8_PATH_MMA_SYNC) == igc.INT8_PATH_TCGEN05
-    assert igc.igc_set_int8_path(2) == -1            # no such path: unchanged
-    assert igc.igc_set_int8_path(igc.INT8_PATH_TCGEN05) == igc.INT8_PATH_MMA_SYNC
+    assert igc.igc_set_int8_path(3) == -1            # no such path: unchanged
+    assert igc.igc_set_int8_path(igc.INT8_PATH_FUSED) == igc.INT8_PATH_MMA_SYNC
+    assert igc.igc_set_int8_path(igc.INT8_PATH_TCGEN05) == igc.INT8_PATH_FUSED
 
 
 def test_stage_depth_setter_roundtrip():

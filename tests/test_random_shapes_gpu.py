@@ -144,7 +144,7 @@ def test_random_sweep_exact_small_integers():
             zA = rng.integers(0, 256, size=M).astype(np.int32)
             zB = int(rng.integers(-128, 128))
             sc = rng.uniform(1e-6, 1e-3, size=N).astype(np.float32)
-            w, path = int(rng.choice([0, 0, 128, 256])), int(rng.choice([0, 0, 0, 1]))
+            w, path = int(rng.choice([0, 0, 128, 256])), int(rng.choice([0, 0, 2, 1]))
             old_w, old_p = igc.igc_set_tile_width(w), igc.igc_set_int8_path(path)
             try:
                 C32 = torch.empty((M, N), dtype=torch.int32, device="cuda")
