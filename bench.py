@@ -300,30 +300,37 @@ def e2e_measure(steps_objs, w3, w4, w5, steps: int, pipelined: bool):
     return ms, h2d, d2h
 
 
-def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 10):
-    """Rows beyond the step (not part of `value`): each timed alone with CUDA events,
-    L2 flushed before every iteration, median of `iters`.  After the flush a spin
-    kernel (about 100 us) keeps the GPU busy while the host enqueues the timed call,
-    so that the events bracket device time only (the call's host-side cost, about
-    10 us through the Python binding, is in the e2e figure, not in these rows)."""
+def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 40):
+    """Rows beyond the step (not part of `value`), each timed alone on the device.
+
+    Every call runs after an L2 flush and a spin kernel (about 50 us) that keeps
+    the GPU busy while the host enqueues the call, so host-side cost is left out.
+    CUDA-event timestamps on GB300 come in steps of about 2 us, too coarse for one
+    call of a few microseconds, so a row's time is measured as the difference of
+    two event-timed runs of `iters` iterations, (flush, spin, call) and (flush,
+    spin), divided by `iters`: the median of three such differences."""
     import torch
     import implicit_gemm_conv_tcgen05_gb300 as igc
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
+    def block_ms(fn, n):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(n):
+            flush.zero_()
+            torch.cuda._sleep(100_000)
+            if fn is not None:
+                fn()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e)
+
     def t_ms(fn):
         fn()
         torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ts = []
-        for _ in range(iters):
-            flush.zero_()
-            torch.cuda._sleep(200_000)
-            s.record()
-            fn()
-            e.record()
-            e.synchronize()
-            ts.append(s.elapsed_time(e))
-        return float(np.median(ts))
+        d = [(block_ms(fn, iters) - block_ms(None, iters)) / iters for _ in range(3)]
+        return float(np.median(d))
 
     def graph_ms(fn, n=100, reps=5):
         """Per-call time of n calls captured in one CUDA graph (median of reps replays)."""
@@ -599,10 +606,12 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_extras:
         result["extras"] = extras_measure(device, peak_burst, hbm)
-        result["extras_note"] = ("rows beyond the step, each timed alone on the device (L2 "
-                                 "flushed, host enqueue hidden behind a spin kernel, median of "
-                                 "10; *_graph100 rows: per-call time of 100 launches replayed "
-                                 "from a CUDA graph, L2 warm); not part of value")
+        result["extras_note"] = ("rows beyond the step, each timed alone on the device: L2 "
+                                 "flushed and the host enqueue hidden behind a spin kernel before "
+                                 "every call, per-call time = (40 x (flush, spin, call) - 40 x "
+                                 "(flush, spin)) / 40, median of 3, since single event pairs "
+                                 "resolve about 2 us; *_graph100 rows: per-call time of 100 "
+                                 "launches replayed from a CUDA graph, L2 warm); not part of value")
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w3, w4, w5, target_s=args.cpu_seconds)

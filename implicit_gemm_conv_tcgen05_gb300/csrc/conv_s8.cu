@@ -73,6 +73,8 @@ static __global__ void __launch_bounds__(256) pad_shift_pixels_kernel(
     const uint8_t* __restrict__ x, int is_signed, int offset, int border, int N, int H, int W,
     int C, int ph, int pw, int Hp, int Wp, int vec, __half* __restrict__ xp,
     int32_t* __restrict__ px) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const long long pixel = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = static_cast<int>(threadIdx.x % 32);
   const long long npix = static_cast<long long>(N) * Hp * Wp;
@@ -135,6 +137,8 @@ static __global__ void __launch_bounds__(256) pad_shift_chunks_kernel(
     const uint8_t* __restrict__ x, uint32_t flip, int border, int N, int H, int W, int C, int ph,
     int pw, int Hp, int Wp, int log2g, __half* __restrict__ xp, int32_t* __restrict__ px,
     unsigned w_blocks, const PrepassOperand wop, int wK, int wKp) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   if (blockIdx.x < w_blocks) {
     const int row = static_cast<int>(blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32);
     if (row < wop.rows) widen_row(wop, row, wK, wKp, static_cast<int>(threadIdx.x % 32));
@@ -183,6 +187,8 @@ static __global__ void __launch_bounds__(256) window_sums_kernel(const int32_t* 
                                                           int Hp, int Wp, int P, int Q, int R,
                                                           int S, int sh, int sw,
                                                           int32_t* __restrict__ rx) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const long long m = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long M = static_cast<long long>(N) * P * Q;
   if (m >= M) return;
@@ -270,7 +276,7 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
       const long long pix_blocks = (threads + 255) / 256;
       const long long w_blocks = (static_cast<long long>(K) + 7) / 8;  // 8 weight rows per block
       if (pix_blocks + w_blocks >= (1LL << 31)) return IGC_ERR_UNSUPPORTED;
-      rc = launch_plain(pad_shift_chunks_kernel, dim3(static_cast<unsigned>(pix_blocks + w_blocks)),
+      rc = launch_pdl(pad_shift_chunks_kernel, dim3(static_cast<unsigned>(pix_blocks + w_blocks)),
                       dim3(256), 0, stream, static_cast<const uint8_t*>(x),
                       x_signed ? 0x80808080u : 0u, zX - oX, N, H, W, C, pad_h, pad_w,
                       static_cast<int>(c.Hp), static_cast<int>(c.Wp), log2g, xp, px,
@@ -278,7 +284,7 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
                       static_cast<int>(c.Kgp));
       weights_done = true;
     } else {
-      rc = launch_plain(pad_shift_pixels_kernel, dim3(static_cast<unsigned>((npix + 7) / 8)),
+      rc = launch_pdl(pad_shift_pixels_kernel, dim3(static_cast<unsigned>((npix + 7) / 8)),
                       dim3(256), 0, stream, static_cast<const uint8_t*>(x), x_signed ? 1 : 0, oX,
                       zX - oX, N, H, W, C, pad_h, pad_w, static_cast<int>(c.Hp),
                       static_cast<int>(c.Wp), vec, xp, px);
@@ -294,7 +300,7 @@ extern "C" int conv2d_nhwc_s8_zp(int N, int H, int W, int C, int K, int R, int S
   //    sums the pixel sums itself (R*S loads per output row, from L2)
   const bool sums_in_epilogue = R * S <= kEpilogueWindowMax;
   if (!sums_in_epilogue) {
-    rc = launch_plain(window_sums_kernel, dim3(static_cast<unsigned>((c.M + 255) / 256)),
+    rc = launch_pdl(window_sums_kernel, dim3(static_cast<unsigned>((c.M + 255) / 256)),
                     dim3(256), 0, stream, static_cast<const int32_t*>(px), N,
                     static_cast<int>(c.Hp), static_cast<int>(c.Wp), static_cast<int>(c.P),
                     static_cast<int>(c.Q), R, S, stride_h, stride_w, rx);

@@ -235,6 +235,8 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
+  grid_dependency_wait();  // programmatic dependent launch, as in gemm_tc.cuh
+  grid_dependents_launch();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
   const uint32_t peer_base = ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), peer));

@@ -285,13 +285,15 @@ int launch_i8(const DeviceInfo& dev, const CUtensorMap& tmA, const void* Bt, int
   cfg.blockDim = dim3(kI8Threads, 1, 1);
   cfg.dynamicSmemBytes = I8Cfg<BN>::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, igc_i8_gemm_kernel<BN, kDequant>, tmA, tmB, tmBh, om.map[0], om.map[1],
                          om.map[2], p, flipA, flipB) != cudaSuccess) {
     (void)cudaGetLastError();

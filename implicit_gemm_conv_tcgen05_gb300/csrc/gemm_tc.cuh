@@ -1026,6 +1026,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
+  // Set-up above touches no global memory; from here on the previous kernel in
+  // the stream must have finished (programmatic dependent launch).
+  grid_dependency_wait();
+  grid_dependents_launch();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t lim = p.wait_limit_ns;
   // The pair's MMAs write both CTAs' tensor memory at the leader's address: both

@@ -56,18 +56,22 @@ int encode_im2col_nhwc(CUtensorMap* map, const void* base, int N, int H, int W, 
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Launches a non-cluster kernel on `stream` (cudaLaunchKernelEx, no launch
-// attributes); returns IGC_OK or IGC_ERR_CUDA.
+// Launches a non-cluster kernel with programmatic stream serialization: it may
+// start while the previous kernel in the stream runs and waits for it in the
+// kernel (griddepcontrol.wait) before touching memory.
 template <typename... Params, typename... Args>
-int launch_plain(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
-                 cudaStream_t stream, Args&&... args) {
+int launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...) != cudaSuccess) {
     (void)cudaGetLastError();
     return IGC_ERR_CUDA;

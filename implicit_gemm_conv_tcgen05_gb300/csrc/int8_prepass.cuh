@@ -105,6 +105,8 @@ static __device__ __forceinline__ void widen_row(const PrepassOperand& o, int ro
 
 // Both operands of a GEMM go through one launch: rows of op[0], then of op[1].
 static __global__ void __launch_bounds__(256) shift_widen_rowsum_kernel(const PrepassParams pp) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   int row = blockIdx.x * (blockDim.x / 32) + static_cast<int>(threadIdx.x / 32);
   const int lane = static_cast<int>(threadIdx.x % 32);
   // select the operand field by field (a dynamic index into the parameter
@@ -147,7 +149,7 @@ inline int launch_prepass(const PrepassOperand* ops, int n_ops, long long K, lon
   pp.Kp = static_cast<int>(Kp);
   const long long rows = static_cast<long long>(pp.op[0].rows) + (n_ops > 1 ? pp.op[1].rows : 0);
   const long long blocks = (rows + 7) / 8;
-  return launch_plain(shift_widen_rowsum_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+  return launch_pdl(shift_widen_rowsum_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
                     stream, pp);
 }
 

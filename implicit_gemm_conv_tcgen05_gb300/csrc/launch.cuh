@@ -127,17 +127,15 @@ int launch_tc_gemm(const DeviceInfo& dev, const CUtensorMap& tmA, const CUtensor
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = TileCfg<BN, ATOMS>::kSmemBytes;
   cfg.stream = stream;
-  // Plain stream order.  Programmatic dependent launch (starting the set-up
-  // while the previous kernel finishes) was measured on GB300: no gain in the
-  // back-to-back GEMM / convolution step, and an isolated small call after
-  // another kernel took 8.8 us instead of 2.4 us.
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, igc_tc_gemm_kernel<kMode, BN, ATOMS>, tmA, tmB, tmBh, om.map[0],
                          om.map[1], om.map[2], p) != cudaSuccess) {
     (void)cudaGetLastError();

@@ -128,6 +128,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// running; it must wait here before touching memory that kernel writes or
+// reads.  The trigger lets the next kernel start its own set-up early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), completion signalled on an mbarrier
 // ---------------------------------------------------------------------------
 // Brings the 128-byte line holding global address `a` into L2 (no register result).

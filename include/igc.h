@@ -38,9 +38,11 @@
  *    schedule of a call depends only on its arguments and the device, unless
  *    the calling thread itself forced one through the test hooks of
  *    igc_debug.h (thread-local: they never reach another thread's calls).
- *  - Launch: plain stream-ordered kernel launches.  Calls may be captured in
- *    CUDA graphs; make one call of each operation on the device first
- *    (per-kernel set-up runs once, outside the capture).
+ *  - Launch: kernels use programmatic dependent launch -- a kernel may start
+ *    while the previous kernel in the stream finishes, and waits for it before
+ *    touching memory -- so stream order is kept as with plain launches.  Calls
+ *    may be captured in CUDA graphs; make one call of each operation on the
+ *    device first (per-kernel set-up runs once, outside the capture).
  */
 #ifndef IGC_H
 #define IGC_H
