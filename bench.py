@@ -357,6 +357,21 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 40):
 
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
     out = {}
+    # the step's fp16 GEMM and convolution, each timed alone (in the step they follow
+    # the int8 GEMM and run under the power cap it leaves)
+    w3 = synth.workload(3)
+    A, B = t(w3["A"]), t(w3["Bt"])
+    C = torch.empty((4096, 4096), dtype=torch.float16, device=device)
+    ms = t_ms(lambda: igc.gemm_f16(A, B, C))
+    out["gemm_f16_4096^3_alone"] = {"ms": ms, "tflops": OPS["gemm_f16_4096"] / ms / 1e9}
+    del A, B, C, w3
+    w4 = synth.workload(4)
+    x, w = t(w4["x"]), t(w4["w"])
+    y = torch.empty((256, 14, 14, 512), dtype=torch.float16, device=device)
+    ms = t_ms(lambda: igc.conv2d_nhwc_f16_implicit(x, w, y, pad=(1, 1)))
+    out["conv3x3_256x14x14x256->512_alone"] = {
+        "ms": ms, "tflops": OPS["conv3x3_256x14x14x256_512"] / ms / 1e9}
+    del x, w, y, w4
     # bf16 GEMM 4096^3, bf16 out
     A = t(synth.normal_bf16_bits(41, 1, (4096, 4096)).view(np.int16)).view(torch.bfloat16)
     B = t(synth.normal_bf16_bits(41, 2, (4096, 4096)).view(np.int16)).view(torch.bfloat16)
@@ -386,6 +401,14 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 40):
     finally:
         igc.igc_set_int8_path(old_path)
     out["gemm_s8_zp_8192^3_mma_sync_path"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
+    # the same on the fused path (operands widened inside the GEMM kernel, no pre-pass)
+    old_path = igc.igc_set_int8_path(igc.INT8_PATH_FUSED)
+    try:
+        ms = t_ms(lambda: igc.gemm_s8_zp(Aq, Bq, zA_row=zA, C8=C8w, scale_col=scol,
+                                         workspace=ws))
+    finally:
+        igc.igc_set_int8_path(old_path)
+    out["gemm_s8_zp_8192^3_fused_path"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
     del Aq, Bq, Y, ws, C8w
     # int8 convolution on the layer shape: x uint8 NHWC 256x14x14x256, w int8 512x3x3x256
     x8 = t(synth.uniform_int(43, 6, (256, 14, 14, 256), 0, 255, np.uint8))
@@ -443,6 +466,15 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 40):
     out["gemm_s8_zp_1024^3_c32_c8"] = {"ms": ms, "tops": 2 * 1024 ** 3 / ms / 1e9,
                                        **roofline_fields(2.0 * 1024 ** 3, BYTES["gemm_s8_zp_1024"],
                                                          ms, peak_tflops, hbm_gbs)}
+    old_path = igc.igc_set_int8_path(igc.INT8_PATH_FUSED)
+    try:
+        ms = t_ms(lambda: igc.gemm_s8_zp(A2, B2, zA=128, zB=121, C32=C32, C8=C8,
+                                         scale=w2["scale"], workspace=ws2))
+    finally:
+        igc.igc_set_int8_path(old_path)
+    out["gemm_s8_zp_1024^3_c32_c8_fused_path"] = {
+        "ms": ms, "tops": 2 * 1024 ** 3 / ms / 1e9,
+        **roofline_fields(2.0 * 1024 ** 3, BYTES["gemm_s8_zp_1024"], ms, peak_tflops, hbm_gbs)}
     # the same two calls as 100 back-to-back launches replayed from a CUDA graph
     # (no host launch cost; inputs stay in L2 between the launches)
     ms = graph_ms(lambda: igc.gemm_f16(A1, B1, C1))
