@@ -96,3 +96,75 @@ def test_three_int8_paths_agree_bit_for_bit():
     o32, o8 = _oracle(Abuf, Bbuf, K, 1, 0, **kw)
     for g32, g8 in outs:
         assert np.array_equal(g32, o32) and np.array_equal(g8, o8)
+
+
+@pytest.mark.parametrize("M,N,K,signs,width", [
+    (256, 256, 256, (0, 1), 0),
+    (300, 520, 1100, (1, 0), 0),
+    (2560, 2048, 320, (0, 0), 256),
+    (130, 200, 96, (1, 1), 128),
+])
+def test_fused_dequantised_output_bit_exact(M, N, K, signs, width):
+    """gemm_s8_zp_dequant on the fused path: Y = ((fp32(C32) s_row) s_col) + bias,
+    bit for bit against the oracle's dequantisation of its own C32."""
+    import synth
+    a_signed, b_signed = signs
+    rng = np.random.default_rng(7 * M + N + K)
+    Abuf, Bbuf, _ = _operands(rng, M, N, K, a_signed, b_signed)
+    zA_row = rng.integers(0, 200, size=M).astype(np.int32)
+    zB = int(rng.integers(-10, 130))
+    s_row = synth.uniform_f32(M + K, 5, (M,), 1e-3, 1e-1)
+    s_col = synth.uniform_f32(N + K, 6, (N,), 1e-3, 1e-1)
+    bias = synth.uniform_f32(M + N, 7, (N,), -5.0, 5.0)
+    A = torch.from_numpy(Abuf).cuda()[:, :K]
+    Bt = torch.from_numpy(Bbuf).cuda()[:, :K]
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    old_p, old_w = igc.igc_set_int8_path(igc.INT8_PATH_FUSED), igc.igc_set_tile_width(width)
+    try:
+        Y = igc.gemm_s8_zp_dequant(A, Bt, zA_row=d(zA_row), zB=zB, scale_row=d(s_row),
+                                   scale_col=d(s_col), bias=d(bias))
+    finally:
+        igc.igc_set_int8_path(old_p)
+        igc.igc_set_tile_width(old_w)
+    check_device_ok()
+    C32, _, _, _ = oracle.gemm_s8_zp(Abuf[:, :K], Bbuf[:, :K], a_signed=a_signed,
+                                     b_signed=b_signed, zA_row=zA_row, zB=zB, want_c8=False)
+    want = oracle.dequant_matrix(C32, s_row, s_col, bias)
+    got = host(Y)
+    bad = np.count_nonzero(got.view(np.uint32) != want.view(np.uint32))
+    assert bad == 0, f"{bad} of {got.size} dequantised outputs differ"
+
+
+def test_fused_path_in_a_cuda_graph_with_new_inputs():
+    """The fused kernel captured in a CUDA graph and replayed after the inputs
+    changed in place gives the new inputs' results."""
+    rng = np.random.default_rng(91)
+    M, N, K = 512, 640, 768
+    A = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    Bt = torch.empty((N, K), dtype=torch.int8, device="cuda")
+    C32 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    C8 = torch.empty((M, N), dtype=torch.int8, device="cuda")
+    kw = dict(zA=100, zB=3, scale=2.0 ** -11)
+    old = igc.igc_set_int8_path(igc.INT8_PATH_FUSED)
+    try:
+        igc.gemm_s8_zp(A.zero_(), Bt.zero_(), C32=C32, C8=C8, **kw)  # set-up outside capture
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                igc.gemm_s8_zp(A, Bt, C32=C32, C8=C8, **kw)
+        torch.cuda.current_stream().wait_stream(side)
+        for trial in range(2):
+            Ah = rng.integers(0, 256, (M, K)).astype(np.uint8)
+            Bh = rng.integers(-128, 128, (N, K)).astype(np.int8)
+            A.copy_(torch.from_numpy(Ah))
+            Bt.copy_(torch.from_numpy(Bh))
+            g.replay()
+            check_device_ok()
+            o32, o8 = _oracle(Ah, Bh, K, 0, 1, **kw)
+            assert np.array_equal(host(C32), o32), f"C32 differs on replay {trial}"
+            assert np.array_equal(host(C8), o8), f"C8 differs on replay {trial}"
+    finally:
+        igc.igc_set_int8_path(old)
