@@ -43,9 +43,13 @@
 // 592 us for the pre-pass + GEMM path (IGC_INT8_PATH_TCGEN05).  With the
 // conversion taken out (barrier protocol and int8 TMA only) the kernel takes
 // 500 us, less than the pre-pass path's GEMM (532 us), since int8 tiles move
-// half the bytes; the conversion itself is what costs: every tile converts its
-// own A and B panels, 4.3 GB of int8 for 128 MB of distinct operand bytes,
-// about 1.8 instructions per byte on four converter warps per SM.
+// half the bytes.  Two costs then hold it near twice the MMA time each: the
+// shared-memory stores of the fp16 stages beside the tensor cores' and TMA's
+// traffic (stores alone: 902 us), and the conversion arithmetic on four
+// converter warps per SM (every tile converts its own A and B panels, 4.3 GB of
+// int8 for 128 MB of distinct operand bytes, about 1.8 instructions per byte).
+// The BN = 256 instantiations spill a few words (ptxas: 24-36 bytes) at this
+// register split; the epilogue needs its 208 and the converters their 64.
 #pragma once
 
 #include "gemm_tc.cuh"
