@@ -81,10 +81,10 @@ constexpr int kEpiWarps = 8;
 // Three warpgroups: warps 0-3 (TMA producer, MMA issuer / TMEM owner, two prefetch)
 // and two epilogue warpgroups (warps 4-11).  After set-up the first warpgroup
 // gives registers to the epilogue ones (setmaxnreg): kRegsLow + 2 kRegsHigh
-// warpgroup shares = 56 * 128 + 216 * 256 = 62464 registers, which fits the
+// warpgroup shares = 72 * 128 + 216 * 256 = 64512 registers, exactly the
 // launch's 384 threads x kMinLaunchRegs (checked on the host before launch).
 constexpr int kThreads = 128 + 32 * kEpiWarps;  // 384
-constexpr int kRegsLow = 56;
+constexpr int kRegsLow = 72;
 constexpr int kRegsHigh = 216;
 constexpr int kMinLaunchRegs = 168;
 static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kThreads * kMinLaunchRegs, "register split");
@@ -313,6 +313,59 @@ __device__ __forceinline__ Unit unit_coords(const KParams& p, int u) {
   }
   tile_coords(p, t, w.mb, w.nb);
   return w;
+}
+
+// First B row (output column) this CTA loads for unit w: each CTA holds half of
+// the unit's B rows at the start of its stage buffer; a half unit's BN/4 rows
+// come through tmBh, whose box is BN/4 rows.
+template <int BN>
+__device__ __forceinline__ int b_row0(const Unit& w, uint32_t rank) {
+  return w.half ? w.nb * BN + w.j * (BN / 2) + static_cast<int>(rank) * (BN / 4)
+                : w.nb * BN + static_cast<int>(rank) * (BN / 2);
+}
+
+// The CTA's first unit u, worked out by one thread during the set-up (integer
+// divisions, first parameter reads) instead of in front of the producer's first
+// copies, and left in first_unit[0..3] (shared memory).
+__device__ __forceinline__ void store_first_unit(const KParams& p, int u, int* first_unit) {
+  const Unit w = unit_coords(p, u);
+  first_unit[0] = w.mb;
+  first_unit[1] = w.nb;
+  first_unit[2] = w.j;
+  first_unit[3] = w.half ? 1 : 0;
+}
+
+__device__ __forceinline__ Unit load_first_unit(const int* first_unit) {
+  Unit w;
+  w.mb = first_unit[0];
+  w.nb = first_unit[1];
+  w.j = first_unit[2];
+  w.half = first_unit[3] != 0;
+  return w;
+}
+
+// L2 prefetch (TMA boxes) of the first n_stages pipeline stages of the CTA's
+// first unit (store_first_unit), by one thread during the set-up, so that the
+// first copies after it find their tiles in L2 instead of DRAM.  A prefetch
+// makes nothing visible to the kernel, so it may run before the grid dependency
+// wait: L2 stays coherent with the previous kernel's writes.  Not inlined: it
+// runs once, and kept out of the kernel body its values stay out of the
+// producer's register budget.
+template <int BN, int ATOMS>
+__device__ __noinline__ void prefetch_first_stages(const KParams& p, const CUtensorMap* tmA,
+                                                   const CUtensorMap* tmB,
+                                                   const CUtensorMap* tmBh,
+                                                   const int* first_unit, uint32_t rank,
+                                                   int n_stages) {
+  const Unit w = load_first_unit(first_unit);
+  const int m_cta = w.mb * BM + static_cast<int>(rank) * BM_CTA;
+  const int n_cta = b_row0<BN>(w, rank);
+  const CUtensorMap* mapB = w.half ? tmBh : tmB;
+  const int atoms = (p.num_kb < n_stages ? p.num_kb : n_stages) * ATOMS;
+  for (int j = 0; j < atoms; ++j) {
+    tma_prefetch_2d(tmA, j * BK, m_cta);
+    tma_prefetch_2d(mapB, j * BK, n_cta);
+  }
 }
 
 // L2 prefetch of k bytes [k0, k0 + kb) of `nrows` operand rows from row0 (rows
@@ -753,9 +806,9 @@ __device__ __forceinline__ void float_group(const KParams& p, const IntRow& r,
 // of the warp must call it and run every group: the column values are broadcast
 // by shuffles and the TMA paths are warp-collective; only the direct stores are
 // predicated on the row.
-// store_row_int_v takes the row terms and the column vectors ready-made (the
-// kernel that converts its operands itself takes the sums from shared memory);
-// store_row_int reads them from global memory.
+// The row terms r and the column vectors V come ready-made: the pre-pass
+// kernels' epilogue reads them from global memory (epi_int_unit), the kernel
+// that converts its operands itself takes the sums from shared memory.
 // kDequant false: the caller guarantees p.yf == nullptr (no dequantised output),
 // which drops that output's code and registers.
 template <int NC, bool kDequant = true>
@@ -854,17 +907,6 @@ __device__ __forceinline__ void store_row_int_v(const KParams& p, const CUtensor
   }
 }
 
-template <int NC>
-__device__ __forceinline__ void store_row_int(const KParams& p, const CUtensorMap& tmO0,
-                                              const CUtensorMap& tmO1, const CUtensorMap& tmO2,
-                                              const Stager& st, int m, int n0,
-                                              const uint32_t (&sum)[NC]) {
-  const IntRow r = int_row(p, m);
-  ColVecs<NC> V;
-  load_col_vecs<NC>(p, n0, st.lane, V);
-  store_row_int_v<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum, r, V);
-}
-
 // Loads NC consecutive TMEM columns (this warp's 32 lanes) into v: 32 columns
 // per tcgen05.ld, then 16 for a remainder.  The caller waits (tmem_ld_wait).
 template <int NC>
@@ -951,6 +993,56 @@ __device__ __forceinline__ void epi_float_cols(const KParams& p, const CUtensorM
   if (active) store_row_float<NCX>(p, tmO0, tmO1, st, m, n0, v, nvalid);
 }
 
+// One warp's integer epilogue for a unit: NCX columns of this warp's lanes at
+// TMEM address cols (accumulator 0; accumulator a lies a * acc_stride further),
+// drained chunk by chunk into int32 running sums, each accumulator released
+// (arrival on the leader's tempty) once drained, then row m's outputs at columns
+// n0 .. n0+NCX-1.  kEarly: the row terms and column vectors are read before the
+// first accumulator wait, where their latency hides behind the MMAs; the widest
+// warps (NCX = 128) read them after the drain, when the registers are free.
+// An inactive warp (the idle half of a half unit) only takes part in the
+// releases.  Returns false if a wait gave up.
+template <int NCX, bool kEarly>
+__device__ __forceinline__ bool epi_int_unit(const KParams& p, const CUtensorMap& tmO0,
+                                             const CUtensorMap& tmO1, const CUtensorMap& tmO2,
+                                             const Stager& st, uint32_t cols, uint32_t acc_stride,
+                                             int m, int n0, int n_chunks, bool active,
+                                             uint64_t* tfull,
+                                             uint32_t tempty_lead, int& acc, uint32_t& acc_phase,
+                                             uint64_t lim, volatile int* abort_flag, int lane) {
+  uint32_t sum[NCX];
+  IntRow r;
+  ColVecs<NCX> V;
+  if constexpr (kEarly) {
+    r = int_row(p, m);
+    load_col_vecs<NCX>(p, n0, lane, V);
+  }
+  for (int c = 0; c < n_chunks; ++c) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag, p.status,
+                                            kSiteEpiFull)))
+      return false;
+    tc_fence_after();
+    const uint32_t taddr = cols + static_cast<uint32_t>(acc) * acc_stride;
+    if (active) {
+      if constexpr (NCX % 64 == 0)
+        tmem_drain<NCX>(taddr, sum, c == 0);
+      else
+        tmem_drain_x32<NCX>(taddr, sum, c == 0);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+  if constexpr (!kEarly) {
+    r = int_row(p, m);
+    load_col_vecs<NCX>(p, n0, lane, V);
+  }
+  if (active) store_row_int_v<NCX>(p, tmO0, tmO1, tmO2, st, m, n0, sum, r, V);
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -987,6 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_t + Cfg::kTailStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* progress = abort_flag + 1;  // producer: stages issued (read by the prefetch)
+  int* first_unit = const_cast<int*>(progress) + 1;  // the first unit's Unit fields
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
   const int lane = static_cast<int>(lane_id());
@@ -1023,11 +1116,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc_2cta(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish_2cta();
   }
+  if (warp == 3 && lane == 0) store_first_unit(p, cluster, first_unit);
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+  // barriers of both CTAs initialised, TMEM allocated in both, first unit known
+  cluster_arrive();
+  // Between its arrival and the barrier's completion warp 3 prefetches a floating
+  // GEMM's first stages into L2 (an integer GEMM's operands are written by its
+  // pre-pass, the kernel before it in the stream).  The copy engine may hold the
+  // thread until the tensor maps are fetched, which then delays only this warp.
+  if constexpr (kMode == Mode::GemmF16 || kMode == Mode::GemmBF16)
+    if (warp == 3 && lane == 0)
+      prefetch_first_stages<BN, ATOMS>(p, &tmA, &tmB, &tmBh, first_unit, rank, kStages);
+  cluster_wait();
   tc_fence_after();
-  // Set-up above touches no global memory; from here on the previous kernel in
-  // the stream must have finished (programmatic dependent launch).
+  // Set-up above reads and writes no global memory (an L2 prefetch makes nothing
+  // visible); from here on the previous kernel in the stream must have finished
+  // (programmatic dependent launch).
   grid_dependency_wait();
   grid_dependents_launch();
   const uint32_t tmem_base = *tmem_slot;
@@ -1058,13 +1162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a convolution's stages walk the channel blocks of each filter tap in turn
     const int tap_end = p.conv_cblocks * Cfg::kKS;
     for (int u = cluster; u < p.num_units; u += num_clusters) {
-      const Unit w = unit_coords(p, u);
+      const Unit w = u == cluster ? load_first_unit(first_unit) : unit_coords(p, u);
       const int mb = w.mb;
       const int m_cta = mb * BM + static_cast<int>(rank) * BM_CTA;
-      // each CTA holds half of the unit's B rows at the start of its stage buffer;
-      // a half unit's BN/4 rows come through tmBh, whose box is BN/4 rows
-      const int n_cta = w.half ? w.nb * BN + w.j * (BN / 2) + static_cast<int>(rank) * (BN / 4)
-                               : w.nb * BN + static_cast<int>(rank) * Cfg::kBNHalf;
+      const int n_cta = b_row0<BN>(w, rank);
       const CUtensorMap* mapB = w.half ? &tmBh : &tmB;
       const uint32_t stage_tx =
           2u * (kStageABytes + (w.half ? Cfg::kStageBBytes / 2 : Cfg::kStageBBytes));
@@ -1274,9 +1375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // tcgen05.ld: warp w may access lanes 32*(w%4) .. +31
     const int half = ew >> 2;   // which column half of the tile
     const int row_in_cta = quad * 32 + lane;
-    // TMEM address of this warp's lanes and column half (integer modes)
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                               static_cast<uint32_t>(half * NC);
+    // TMEM address of this warp's lanes, accumulator 0, column 0
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     const int n_chunks = (p.num_kb + p.chunk_kb - 1) / p.chunk_kb;
     Stager st;
     st.buf = staging + ew * kStagingWarpBytes;
@@ -1288,10 +1388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = cluster; u < p.num_units; u += num_clusters) {
       const Unit w = unit_coords(p, u);
       const int m = w.mb * BM + static_cast<int>(rank) * BM_CTA + row_in_cta;
-      // a half unit's NC columns are handled by the half-0 warps alone; the
-      // others only take part in the accumulator hand-offs
+      // A whole tile's warps take NC columns each (warpgroup `half` the tile's
+      // column half); a half unit's BN/2 columns are split the same way, NC/2
+      // per warp, except at BN = 224 and in the integer modes' BN = 256, where the
+      // half-0 warps take all of them and the others only take part in the
+      // accumulator hand-offs.
       const bool active = !w.half || half == 0;
       const int n0 = w.half ? w.nb * BN + w.j * NC : w.nb * BN + half * NC;
+      const int n0h = w.nb * BN + w.j * NC + half * (NC / 2);  // split half unit
       st.row0 = m - lane;
       if constexpr (!mode_is_int(kMode)) {
         if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag,
@@ -1311,28 +1415,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nvalid = w.half ? BN / 2 : (half == 0 ? 128 : BN - 128);
           epi_float_cols<128>(p, tmO0, tmO1, st, acc_cols + static_cast<uint32_t>(col), m,
                               w.half ? n0 : w.nb * BN + col, nvalid, active, rel, lane);
+        } else if (w.half) {
+          epi_float_cols<NC / 2>(p, tmO0, tmO1, st,
+                                 acc_cols + static_cast<uint32_t>(half * (NC / 2)), m, n0h,
+                                 NC / 2, true, rel, lane);
         } else {
           epi_float_cols<NC>(p, tmO0, tmO1, st, acc_cols + static_cast<uint32_t>(half * NC), m,
-                             n0, NC, active, rel, lane);
+                             n0, NC, true, rel, lane);
         }
       } else {
-        uint32_t sum[NC];
-#pragma unroll
-        for (int i = 0; i < NC; ++i) sum[i] = 0u;
-        for (int c = 0; c < n_chunks; ++c) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag,
-                                                          p.status, kSiteEpiFull)))
-            goto epi_done;
-          tc_fence_after();
-          if (active)
-            tmem_drain<NC>(lane_base + static_cast<uint32_t>(acc) * Cfg::kAccStride, sum, c == 0);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(tempty_lead + static_cast<uint32_t>(acc) * 8u);
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
+        // (two inlined copies of the widest epilogue would not fit the registers:
+        // at NC = 128 a half unit keeps the half-0 warps alone)
+        bool ok;
+        if constexpr (NC <= 64) {
+          ok = w.half ? epi_int_unit<NC / 2, true>(
+                            p, tmO0, tmO1, tmO2, st,
+                            lane_base + static_cast<uint32_t>(half * (NC / 2)), Cfg::kAccStride,
+                            m, n0h, n_chunks, true, tfull, tempty_lead, acc, acc_phase, lim,
+                            abort_flag, lane)
+                      : epi_int_unit<NC, true>(
+                            p, tmO0, tmO1, tmO2, st, lane_base + static_cast<uint32_t>(half * NC),
+                            Cfg::kAccStride, m, n0, n_chunks, true, tfull, tempty_lead, acc,
+                            acc_phase, lim, abort_flag, lane);
+        } else {
+          ok = epi_int_unit<NC, false>(p, tmO0, tmO1, tmO2, st,
+                                       lane_base + static_cast<uint32_t>(half * NC),
+                                       Cfg::kAccStride, m, n0, n_chunks, active, tfull,
+                                       tempty_lead, acc, acc_phase, lim, abort_flag, lane);
         }
-        if (active) store_row_int<NC>(p, tmO0, tmO1, tmO2, st, m, n0, sum);
+        if (!ok) goto epi_done;
       }
     }
   epi_done:
