@@ -225,7 +225,7 @@ def igc_set_stage_depth(k: int) -> int:
     return int(lib().igc_set_stage_depth(int(k)))
 
 
-INT8_PATH_TCGEN05, INT8_PATH_MMA_SYNC, INT8_PATH_FUSED = 0, 1, 2
+INT8_PATH_TCGEN05, INT8_PATH_MMA_SYNC, INT8_PATH_FUSED, INT8_PATH_CONVERT = 0, 1, 2, 3
 
 
 def igc_set_int8_path(path: int) -> int:

@@ -276,7 +276,7 @@ int igc_set_stage_depth(int k) {
 
 int igc_set_int8_path(int path) {
   if (path != IGC_INT8_PATH_TCGEN05 && path != IGC_INT8_PATH_MMA_SYNC &&
-      path != IGC_INT8_PATH_FUSED)
+      path != IGC_INT8_PATH_FUSED && path != IGC_INT8_PATH_CONVERT)
     return -1;
   const int old = igc::t_int8_path;
   igc::t_int8_path = path;

@@ -35,18 +35,28 @@ constexpr size_t kWsAlign = 256;
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline long long k_padded(long long K) { return (K + 7) / 8 * 8; }  // 16-byte fp16 rows
 
+// The fp16 operands and their row sums (written by the pre-pass, or by the
+// converting kernel, which accumulates the sums chunk by chunk), then the
+// converting kernel's flags (one per 128-row block and 1024-k chunk, one per
+// block) and job counter.  The converting kernel's sums, flags and counter are
+// zeroed before each of its launches (one memset from ra_off to the end).
 struct WsLayout {
-  size_t a_off, b_off, ra_off, cb_off, total;
+  size_t a_off, b_off, ra_off, cb_off, flags_off, flags_bytes, total;
 };
 
 WsLayout ws_layout(long long M, long long N, long long K) {
   const long long Kp = k_padded(K);
+  const long long chunks = (K + kCvChunk - 1) / kCvChunk;
+  const long long blocks =
+      (M + kCvBlockRows - 1) / kCvBlockRows + (N + kCvBlockRows - 1) / kCvBlockRows;
   WsLayout l;
   l.a_off = 0;
   l.b_off = l.a_off + align_up(static_cast<size_t>(M) * Kp * 2, kWsAlign);
   l.ra_off = l.b_off + align_up(static_cast<size_t>(N) * Kp * 2, kWsAlign);
   l.cb_off = l.ra_off + align_up(static_cast<size_t>(M) * 4, kWsAlign);
-  l.total = l.cb_off + align_up(static_cast<size_t>(N) * 4, kWsAlign);
+  l.flags_off = l.cb_off + align_up(static_cast<size_t>(N) * 4, kWsAlign);
+  l.flags_bytes = static_cast<size_t>(blocks * chunks + blocks + 1) * 4;
+  l.total = l.flags_off + align_up(l.flags_bytes, kWsAlign);
   return l;
 }
 
@@ -118,11 +128,16 @@ struct DequantOut {
   const float* bias = nullptr;
 };
 
+// The GEMM kernel over the workspace's fp16 operands.  With A_raw set (the
+// converting path: K a multiple of 16, both operands 16-byte aligned with row
+// strides lda, ldb that are multiples of 16) the kernel converts A_raw / Bt_raw
+// itself; otherwise the pre-pass has written the operands and their sums.
 int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, int32_t zA,
                  const int32_t* zA_row, int32_t zB, const int32_t* zB_col, int32_t* C32,
                  int64_t ldc32, int8_t* C8, int64_t ldc8, float scale, const float* scale_col,
                  const DequantOut& dq, const void* workspace, size_t workspace_bytes,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, const void* A_raw = nullptr, int64_t lda = 0,
+                 const void* Bt_raw = nullptr, int64_t ldb = 0) {
   int rc = check_common(M, N, K);
   if (rc != IGC_OK) return rc;
   if (M == 0 || N == 0) return IGC_OK;  // empty output: nothing is read or written
@@ -157,14 +172,42 @@ int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, in
   p.K = static_cast<int>(K);
   p.num_kb = static_cast<int>((Kp + KS - 1) / KS);
   p.chunk_kb = kIntChunkKb;
-  p.pf_a = reinterpret_cast<const char*>(ws + l.a_off);
-  p.pf_lda = Kp * 2;
+  if (A_raw == nullptr) {
+    p.pf_a = reinterpret_cast<const char*>(ws + l.a_off);
+    p.pf_lda = Kp * 2;
+    p.rsumA = reinterpret_cast<const int32_t*>(ws + l.ra_off);
+    p.csumB = reinterpret_cast<const int32_t*>(ws + l.cb_off);
+  } else {
+    uint8_t* wsm = const_cast<uint8_t*>(ws);
+    if (cudaMemsetAsync(wsm + l.ra_off, 0, l.flags_off + l.flags_bytes - l.ra_off, stream) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return IGC_ERR_CUDA;
+    }
+    const long long chunks = (K + kCvChunk - 1) / kCvChunk;
+    p.cv_a = static_cast<const uint8_t*>(A_raw);
+    p.cv_b = static_cast<const uint8_t*>(Bt_raw);
+    p.cv_lda = lda;
+    p.cv_ldb = ldb;
+    p.cv_flip_a = a_signed ? 0x80808080u : 0u;
+    p.cv_flip_b = b_signed ? 0x80808080u : 0u;
+    p.cv_da = reinterpret_cast<__half*>(wsm + l.a_off);
+    p.cv_db = reinterpret_cast<__half*>(wsm + l.b_off);
+    p.cv_sa = reinterpret_cast<int32_t*>(wsm + l.ra_off);
+    p.cv_sb = reinterpret_cast<int32_t*>(wsm + l.cb_off);
+    p.cv_flags = reinterpret_cast<int*>(wsm + l.flags_off);
+    p.cv_blocks_a = static_cast<int>((M + kCvBlockRows - 1) / kCvBlockRows);
+    p.cv_blocks_b = static_cast<int>((N + kCvBlockRows - 1) / kCvBlockRows);
+    p.cv_chunks = static_cast<int>(chunks);
+    const long long blocks = p.cv_blocks_a + p.cv_blocks_b;
+    p.cv_done = p.cv_flags + blocks * chunks;
+    p.cv_queue = p.cv_done + blocks;
+    p.cv_Kp = static_cast<int>(Kp);
+  }
   p.c32 = C32;
   p.ldc32 = ldc32;
   p.c8 = C8;
   p.ldc8 = ldc8;
-  p.rsumA = reinterpret_cast<const int32_t*>(ws + l.ra_off);
-  p.csumB = reinterpret_cast<const int32_t*>(ws + l.cb_off);
   p.zA = zA;
   p.zA_row = zA_row;
   p.zB = zB;
@@ -369,6 +412,13 @@ int run_int_gemm_fused(int64_t M, int64_t N, int64_t K, const void* A, int a_sig
                                         stream);
 }
 
+// The converting path's conditions (IGC_INT8_PATH_CONVERT): 16-byte rows and
+// strides, K a multiple of 16 (so the fp16 rows need no padding).
+bool convert_ok(int64_t K, const void* A, int64_t lda, const void* Bt, int64_t ldb) {
+  return K > 0 && K % 16 == 0 && A != nullptr && Bt != nullptr && lda >= K && ldb >= K &&
+         aligned16(A) && aligned16(Bt) && lda % 16 == 0 && ldb % 16 == 0;
+}
+
 }  // namespace
 
 extern "C" int gemm_s8_zp_run(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed,
@@ -405,6 +455,10 @@ extern "C" int gemm_s8_zp_dequant(int64_t M, int64_t N, int64_t K, const void* A
     return run_int_gemm_fused(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, zA, zA_row, zB,
                               zB_col, nullptr, 0, nullptr, 0, 0.0f, nullptr, dq,
                               reinterpret_cast<cudaStream_t>(stream));
+  if (int8_path_override() == IGC_INT8_PATH_CONVERT && convert_ok(K, A, lda, Bt, ldb))
+    return run_int_gemm(M, N, K, a_signed, b_signed, zA, zA_row, zB, zB_col, nullptr, 0, nullptr,
+                        0, 0.0f, nullptr, dq, workspace, workspace_bytes,
+                        reinterpret_cast<cudaStream_t>(stream), A, lda, Bt, ldb);
   rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,
                           workspace_bytes, stream);
   if (rc != IGC_OK) return rc;
@@ -445,6 +499,10 @@ extern "C" int gemm_s8_zp(int64_t M, int64_t N, int64_t K, const void* A, int a_
     return run_int_gemm_fused(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, zA, zA_row, zB,
                               zB_col, C32, ldc32, C8, ldc8, scale, scale_col, DequantOut(),
                               reinterpret_cast<cudaStream_t>(stream));
+  if (int8_path_override() == IGC_INT8_PATH_CONVERT && convert_ok(K, A, lda, Bt, ldb))
+    return run_int_gemm(M, N, K, a_signed, b_signed, zA, zA_row, zB, zB_col, C32, ldc32, C8,
+                        ldc8, scale, scale_col, DequantOut(), workspace, workspace_bytes,
+                        reinterpret_cast<cudaStream_t>(stream), A, lda, Bt, ldb);
   if (K > 0) {
     if (A == nullptr || Bt == nullptr) return IGC_ERR_INVALID_ARG;
     rc = gemm_s8_zp_prepare(M, N, K, A, a_signed, lda, Bt, b_signed, ldb, workspace,

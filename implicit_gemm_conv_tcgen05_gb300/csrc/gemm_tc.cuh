@@ -59,6 +59,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "int8_widen.cuh"
 #include "sm100_ptx.cuh"
 
 namespace igc {
@@ -91,7 +92,9 @@ static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kThreads * kMinLaunchRegs, "re
 // setmaxnreg.dec only lowers and setmaxnreg.inc only raises a warpgroup's count
 static_assert(kRegsLow <= kMinLaunchRegs && kRegsHigh >= kMinLaunchRegs, "register split direction");
 constexpr uint32_t kAtomABytes = BM_CTA * BK * 2;   // 16 KB
-constexpr uint32_t kBarrierBytes = 512;
+// barriers and small shared state (512 bytes), then the band table of an integer
+// GEMM converting its own operands (kCvBandTab int2 entries)
+constexpr uint32_t kBarrierBytes = 1536;
 // Each epilogue warp stages 32 rows x 128 bytes of output in shared memory (128-byte
 // swizzle, the layout of a TMA box) and writes them with one bulk tensor store.
 constexpr uint32_t kStagingWarpBytes = 32 * 128;
@@ -142,6 +145,7 @@ enum : uint32_t {
   kSiteEpiFull = 4,
   kSiteDrain = 5,
   kSiteTmemMismatch = 6,
+  kSiteCvFlag = 7,
 };
 
 // Tail-ring slot `i` (BN = 256) after the switch from the main ring, whose stages
@@ -279,6 +283,24 @@ struct KParams {
   long long pf_lda, pf_ldb;
   int pf_kbytes;
   int pf_units;
+  // Integer GEMM that converts its own operands (cv_flags != nullptr; see cv_step):
+  // the raw uint8 / int8 operands A and Bt, their conversion into the fp16 operands
+  // that the copies read (row stride cv_Kp), the sums of their rows (accumulated
+  // chunk by chunk), one flag per 128-row block and 1024-k chunk and one per block
+  // (each counting the finished jobs; A's blocks first) and the job counter of the
+  // queue, all zero at launch.  rsumA / csumB are unused then.
+  const uint8_t* cv_a;
+  const uint8_t* cv_b;
+  long long cv_lda, cv_ldb;
+  uint32_t cv_flip_a, cv_flip_b;  // 0 for uint8, 0x80808080 for int8
+  __half* cv_da;
+  __half* cv_db;
+  int32_t* cv_sa;
+  int32_t* cv_sb;
+  int* cv_flags;
+  int* cv_done;
+  int* cv_queue;
+  int cv_blocks_a, cv_blocks_b, cv_chunks, cv_Kp;
 };
 
 __device__ __forceinline__ void tile_coords(const KParams& p, int t, int& mb, int& nb) {
@@ -368,6 +390,323 @@ __device__ __noinline__ void prefetch_first_stages(const KParams& p, const CUten
   }
 }
 
+// ---------------------------------------------------------------------------
+// Integer GEMM converting its own operands (p.cv_flags != nullptr)
+//
+// The raw uint8 / int8 operands are shifted and widened to fp16 once, in jobs of
+// 8 rows x one 1024-k chunk that the CTAs' spare warps take from a queue: the
+// epilogue warps while they wait for an accumulator (between two polls of its
+// barrier, one job at a time, so a drain starts at most a job late) and warps 2-3
+// throughout.  A job writes the fp16 values where the copies read them and each
+// row's chunk sum, then adds one to the flag of its 128-row block and chunk; the
+// producer waits for a block's flag before copying that block's chunk.  Jobs come
+// in bands: band b holds the blocks that the schedule's tiles b*C .. (b+1)*C - 1
+// (C CTA pairs: one round of the persistent schedule) use first, chunk after
+// chunk, so the first round's blocks are ready first, and every block is
+// converted once.  No job waits on anything, so the flags always complete.
+// ---------------------------------------------------------------------------
+constexpr int kCvRows = 8;                                   // rows of one job
+constexpr int kCvBlockRows = 128;                            // rows under one flag
+constexpr int kCvJobsPerFlag = kCvBlockRows / kCvRows;       // 16
+constexpr int kCvChunk = 1024;                               // k under one flag
+constexpr int kCvBandTab = 128;  // bands whose first blocks are tabulated in shared memory
+static_assert(kIntChunkKb * KS == kCvChunk, "a flag's chunk is one accumulation chunk");
+
+// m-tiles / n-tiles of the raster (tile_coords) whose first tile comes before
+// tile U: a group's m-tiles appear in its first gm tiles, the n-tiles in the
+// first group, one every gm tiles.
+__device__ __forceinline__ int cv_mtiles_before(const KParams& p, int U) {
+  const int per_group = p.group_m * p.tiles_n;
+  const int full = U / per_group;
+  const int first_m = full * p.group_m;
+  if (first_m >= p.tiles_m) return p.tiles_m;
+  const int gm = min(p.tiles_m - first_m, p.group_m);
+  return first_m + min(U - full * per_group, gm);
+}
+
+__device__ __forceinline__ int cv_ntiles_before(const KParams& p, int U) {
+  const int gm0 = min(p.tiles_m, p.group_m);
+  return min((U + gm0 - 1) / gm0, p.tiles_n);
+}
+
+// Bands of the schedule: one per round of C CTA pairs.
+__device__ __forceinline__ int cv_num_bands(const KParams& p, int C) {
+  return (p.num_tiles + C - 1) / C;
+}
+
+// Blocks that band b and the bands before it hold: A [0, a), B [0, b) of the
+// returned pair, from the first tile of band b on.
+template <int BN>
+__device__ __forceinline__ int2 cv_blocks_before(const KParams& p, int band, int C) {
+  constexpr int kBnb = BN / kCvBlockRows;  // B blocks per n-tile
+  const long long t = static_cast<long long>(band) * C;
+  const int u = static_cast<int>(t < p.num_tiles ? t : p.num_tiles);
+  return make_int2(min(2 * cv_mtiles_before(p, u), p.cv_blocks_a),
+                   min(kBnb * cv_ntiles_before(p, u), p.cv_blocks_b));
+}
+
+// One job: rows r0 .. r0+7 of operand A (opB false) or Bt, chunk c.  Lane l takes
+// the 16 bytes at 16 l and at 512 + 16 l of each row's chunk; kRowsInFlight rows'
+// loads are in flight at a time (fewer for the warps with fewer registers).  Each
+// row's chunk sum of the shifted values is added to its row sum.  Every lane must
+// call it (the sums are reduced by shuffles).
+template <int kRowsInFlight>
+__device__ __forceinline__ void cv_job(const KParams& p, bool opB, int r0, int c, int lane) {
+  const uint8_t* src = opB ? p.cv_b : p.cv_a;
+  const long long ld = opB ? p.cv_ldb : p.cv_lda;
+  const uint32_t flip = opB ? p.cv_flip_b : p.cv_flip_a;
+  __half* dst = opB ? p.cv_db : p.cv_da;
+  int32_t* sums = opB ? p.cv_sb : p.cv_sa;
+  const int rows = opB ? p.N : p.M;
+  const int k0 = c * kCvChunk;
+  const int kb = min(kCvChunk, p.K - k0);  // bytes of this chunk (a multiple of 16)
+#pragma unroll 1
+  for (int i0 = 0; i0 < kCvRows; i0 += kRowsInFlight) {
+    uint4 raw[kRowsInFlight][2];
+#pragma unroll
+    for (int i = 0; i < kRowsInFlight; ++i) {
+      const int row = r0 + i0 + i;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int k = j * 512 + lane * 16;
+        raw[i][j] = (row < rows && k < kb)
+                        ? __ldcs(reinterpret_cast<const uint4*>(
+                              src + static_cast<long long>(row) * ld + k0 + k))
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsInFlight; ++i) {
+      const int row = r0 + i0 + i;
+      uint32_t usum = 0;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int k = j * 512 + lane * 16;
+        if (row < rows && k < kb) {
+          uint32_t o[8];
+          prepass::widen4(raw[i][j].x, flip, o[0], o[1], usum);
+          prepass::widen4(raw[i][j].y, flip, o[2], o[3], usum);
+          prepass::widen4(raw[i][j].z, flip, o[4], o[5], usum);
+          prepass::widen4(raw[i][j].w, flip, o[6], o[7], usum);
+          uint4* d =
+              reinterpret_cast<uint4*>(dst + static_cast<long long>(row) * p.cv_Kp + k0 + k);
+          __stcs(d, make_uint4(o[0], o[1], o[2], o[3]));
+          __stcs(d + 1, make_uint4(o[4], o[5], o[6], o[7]));
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) usum += __shfl_xor_sync(0xffffffffu, usum, off);
+      // the shifted sum: each byte read contributed u = value + 128
+      if (lane == 0 && row < rows)
+        atomicAdd(sums + row, static_cast<int32_t>(usum - 128u * static_cast<uint32_t>(kb)));
+    }
+  }
+}
+
+// The band that job s belongs to: the last band whose first job is at or before
+// s (s below the total), found by bisection over the bands' first jobs.
+// (tab: the blocks before bands 0 .. nb, worked out once per CTA, when nb < kCvBandTab)
+template <int BN>
+__device__ __forceinline__ int2 cv_blocks_before_t(const KParams& p, const int2* tab, int band,
+                                                   int nb, int C) {
+  return nb < kCvBandTab ? tab[band] : cv_blocks_before<BN>(p, band, C);
+}
+
+template <int BN>
+__device__ __forceinline__ int cv_band_of(const KParams& p, const int2* tab, int s, int nb, int C,
+                                          int jobs_per_block) {
+  int lo = 0, hi = nb - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int2 bb = cv_blocks_before_t<BN>(p, tab, mid, nb, C);
+    if ((bb.x + bb.y) * jobs_per_block <= s)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+enum : int { kCvNone = 0, kCvDid = 1, kCvLater = 2 };
+
+// Does job s (the s-th of all bands, in band order, chunk-major within a band)
+// and publishes it: every lane orders its stores before the copy engine's later
+// reads, and lane 0 adds one to the job's chunk flag and block count (release).
+// Every lane must call it.
+template <int BN, int kRowsInFlight>
+__device__ __forceinline__ void cv_do_job(const KParams& p, const int2* tab, int s, int nb, int C,
+                                          int lane) {
+  const int jobs_per_block = p.cv_chunks * kCvJobsPerFlag;
+  const int band = cv_band_of<BN>(p, tab, s, nb, C, jobs_per_block);
+  const int2 b0 = cv_blocks_before_t<BN>(p, tab, band, nb, C);
+  const int2 b1 = cv_blocks_before_t<BN>(p, tab, band + 1, nb, C);
+  const int na = b1.x - b0.x;
+  const int per_chunk = (na + (b1.y - b0.y)) * kCvJobsPerFlag;
+  const int r = s - (b0.x + b0.y) * jobs_per_block;
+  const int c = r / per_chunk;
+  const int rem = r - c * per_chunk;
+  const int blk = rem / kCvJobsPerFlag;
+  const int jr = rem - blk * kCvJobsPerFlag;
+  const bool opB = blk >= na;
+  const int block = opB ? b0.y + (blk - na) : b0.x + blk;
+  cv_job<kRowsInFlight>(p, opB, block * kCvBlockRows + jr * kCvRows, c, lane);
+  fence_proxy_async_global();
+  __syncwarp();
+  if (lane == 0) {
+    const int gb = opB ? p.cv_blocks_a + block : block;
+    red_release_gpu_add(p.cv_flags + gb * p.cv_chunks + c, 1);
+    red_release_gpu_add(p.cv_done + gb, 1);
+  }
+}
+
+// Jobs of the first band (the first round's blocks), which are needed at once:
+// shared out statically, job j to converting warp j mod W (W = 10 per CTA, the
+// epilogue warps' numbers first and spread over the CTAs), so the start takes no
+// turns on a shared counter.
+__device__ __forceinline__ int cv_first_band_jobs(const int2* tab) {
+  return (tab[1].x + tab[1].y);  // blocks of band 0 (tab[0] is zero)
+}
+
+__device__ __forceinline__ int cv_static_worker(int warp) {
+  // epilogue warps 4..11 -> 0..7, warps 2-3 -> 8-9, times the CTAs
+  const int local = warp >= 4 ? warp - 4 : warp + 6;
+  return local * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+}
+
+// Takes the next job from the queue of the later bands and does it (kCvDid), unless
+// no job is left (kCvNone) or the next job belongs to a band past max_band
+// (kCvLater: blocks the schedule needs more than a round ahead of this CTA's
+// producer are left for later, so that converted blocks do not crowd the working
+// set out of L2 and the conversion traffic spreads over the run).  Every lane must
+// call it.
+template <int BN, int kRowsInFlight>
+__device__ __forceinline__ int cv_step(const KParams& p, const int2* tab, int C, int max_band,
+                                       int lane) {
+  const int nb = cv_num_bands(p, C);
+  const int jobs_per_block = p.cv_chunks * kCvJobsPerFlag;
+  const int total = (p.cv_blocks_a + p.cv_blocks_b) * jobs_per_block;
+  const int first = cv_first_band_jobs(tab) * jobs_per_block;
+  int s = 0;
+  if (lane == 0) {
+    const int next = first + ld_relaxed_gpu(p.cv_queue);
+    if (next >= total)
+      s = -1;
+    else if (max_band < nb - 1 && cv_band_of<BN>(p, tab, next, nb, C, jobs_per_block) > max_band)
+      s = -2;
+    else
+      s = first + atomicAdd(p.cv_queue, 1);
+  }
+  s = __shfl_sync(0xffffffffu, s, 0);
+  if (s == -2) return kCvLater;
+  if (s < 0 || s >= total) return kCvNone;
+  cv_do_job<BN, kRowsInFlight>(p, tab, s, nb, C, lane);
+  return kCvDid;
+}
+
+// The next of this warp's first-band jobs (advancing *next by W); false when its
+// share is done.  Every lane must call it.
+template <int BN, int kRowsInFlight>
+__device__ __forceinline__ bool cv_static_step(const KParams& p, const int2* tab, int C, int& next,
+                                               int lane) {
+  const int jobs_per_block = p.cv_chunks * kCvJobsPerFlag;
+  if (next >= cv_first_band_jobs(tab) * jobs_per_block) return false;
+  cv_do_job<BN, kRowsInFlight>(p, tab, next, cv_num_bands(p, C), C, lane);
+  next += 10 * static_cast<int>(gridDim.x);
+  return true;
+}
+
+// The band a CTA's converters may reach: one round past the unit its producer
+// is copying (its main ring publishes the stages issued in *progress).
+__device__ __forceinline__ int cv_max_band(const KParams& p, const volatile int* progress) {
+  return *progress / p.num_kb + 1;
+}
+
+// The producer's wait (lane 0) until the conversion of flag `flag` is complete,
+// after which its copies are ordered after the converters' stores.  Every lane
+// must call it; false if the wait gave up (bounded like every other wait).
+__device__ __forceinline__ bool cv_wait(const KParams& p, int flag, uint64_t limit_ns,
+                                        volatile int* abort, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    const int* f = p.cv_flags + flag;
+    if (ld_acquire_gpu(f) < kCvJobsPerFlag) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(f) < kCvJobsPerFlag) {
+        if (*abort) {
+          ok = 0;
+          break;
+        }
+        if (globaltimer_ns() - t0 > limit_ns) {
+          *abort = 1;
+          report_status(p.status, kStatusTimeout, kSiteCvFlag);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    fence_proxy_async_global();
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// The producer's waits before the first copy of chunk c of a unit: the CTA's A
+// block (rows m_cta ..) and B block (rows n_cta ..), where they lie inside the
+// operands (rows outside are zero-filled by the copy, nothing to wait for).
+__device__ __forceinline__ bool cv_wait_chunk(const KParams& p, int m_cta, int n_cta, int c,
+                                              uint64_t limit_ns, volatile int* abort, int lane) {
+  if (m_cta < p.M &&
+      !cv_wait(p, (m_cta / kCvBlockRows) * p.cv_chunks + c, limit_ns, abort, lane))
+    return false;
+  if (n_cta < p.N &&
+      !cv_wait(p, (p.cv_blocks_a + n_cta / kCvBlockRows) * p.cv_chunks + c, limit_ns, abort, lane))
+    return false;
+  return true;
+}
+
+// True when every job of the CTA's A and B blocks for this unit is done (the
+// blocks' job counts, read relaxed, made an acquire by a fence): then the unit's
+// copies need no per-chunk waits.  One round trip at the unit's start instead of
+// two acquire loads before every chunk.  Every lane must call it.
+__device__ __forceinline__ bool cv_unit_ready(const KParams& p, int m_cta, int n_cta, int lane) {
+  int ready = 0;
+  if (lane == 0) {
+    const int full = p.cv_chunks * kCvJobsPerFlag;
+    const int a = m_cta < p.M ? ld_relaxed_gpu(p.cv_done + m_cta / kCvBlockRows) : full;
+    const int b =
+        n_cta < p.N ? ld_relaxed_gpu(p.cv_done + p.cv_blocks_a + n_cta / kCvBlockRows) : full;
+    if (a >= full && b >= full) {
+      fence_acq_rel_gpu();
+      fence_proxy_async_global();
+      ready = 1;
+    }
+  }
+  return __shfl_sync(0xffffffffu, ready, 0) != 0;
+}
+
+// Sum over k of the shifted row `row` of A (opB false) or Bt, read after
+// cv_acquire_sums (so not through the read-only cache).
+__device__ __forceinline__ uint32_t cv_sum(const KParams& p, bool opB, int row) {
+  return static_cast<uint32_t>(__ldcg((opB ? p.cv_sb : p.cv_sa) + row));
+}
+
+// Before the epilogue of a unit reads its row and column sums: the job counts of
+// the blocks that hold them, read relaxed (all at once) and made an acquire by one
+// fence.  Every job of those blocks is complete by then (the unit's copies waited
+// for them), each having added its sums before its release.
+template <int NB>
+__device__ __forceinline__ void cv_acquire_sums(const KParams& p, int m, int n0, int lane) {
+  int seen = ld_relaxed_gpu(p.cv_done + (m < p.M ? m : p.M - 1) / kCvBlockRows);
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int n = n0 + 32 * b + lane;
+    seen += ld_relaxed_gpu(p.cv_done + p.cv_blocks_a + (n < p.N ? n : p.N - 1) / kCvBlockRows);
+  }
+  asm volatile("" ::"r"(seen));
+  fence_acq_rel_gpu();
+}
+
+// ---------------------------------------------------------------------------
 // L2 prefetch of k bytes [k0, k0 + kb) of `nrows` operand rows from row0 (rows
 // past rows_total and bytes past kbytes skipped), by the 64 threads t = 0..63
 // of warps 2-3, one 128-byte line each.
@@ -698,7 +1037,15 @@ __device__ __forceinline__ void load_col_vec(const void* base, int n0, int N, in
 template <int NC>
 __device__ __forceinline__ void load_col_vecs(const KParams& p, int n0, int lane,
                                               ColVecs<NC>& V) {
-  load_col_vec(p.csumB, n0, p.N, lane, V.cB);
+  if (p.cv_flags != nullptr) {
+#pragma unroll
+    for (int b = 0; b < ColVecs<NC>::kB; ++b) {
+      const int n = n0 + 32 * b + lane;
+      V.cB[b] = cv_sum(p, true, n < p.N ? n : p.N - 1);
+    }
+  } else {
+    load_col_vec(p.csumB, n0, p.N, lane, V.cB);
+  }
   load_col_vec(p.zB_col, n0, p.N, lane, V.zB);
   load_col_vec(p.scale_col, n0, p.N, lane, V.sc);
   load_col_vec(p.dq_col, n0, p.N, lane, V.dq);
@@ -747,6 +1094,8 @@ __device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
     for (int r = 0; r < p.conv_R; ++r)
       for (int s = 0; s < p.conv_S; ++s)
         rs += static_cast<uint32_t>(__ldg(base + static_cast<size_t>(r) * p.conv_Wp + s));
+  } else if (p.cv_flags != nullptr) {
+    rs = cv_sum(p, false, mm);
   } else {
     rs = static_cast<uint32_t>(__ldg(p.rsumA + mm));
   }
@@ -1001,23 +1350,52 @@ __device__ __forceinline__ void epi_float_cols(const KParams& p, const CUtensorM
 // first accumulator wait, where their latency hides behind the MMAs; the widest
 // warps (NCX = 128) read them after the drain, when the registers are free.
 // An inactive warp (the idle half of a half unit) only takes part in the
-// releases.  Returns false if a wait gave up.
-template <int NCX, bool kEarly>
+// releases.  An integer GEMM converting its own operands: between polls of the
+// accumulator barrier the warp does conversion jobs: its share of the first band
+// (cv_next: its next one), then jobs of the later bands while cv_left (as many as
+// fit before the warp's first accumulator, cv_first and chunk 0; one per chunk
+// after that; cv_left turns false once their queue is empty).  Returns false if a
+// wait gave up.
+template <int BN, int NCX, bool kEarly>
 __device__ __forceinline__ bool epi_int_unit(const KParams& p, const CUtensorMap& tmO0,
                                              const CUtensorMap& tmO1, const CUtensorMap& tmO2,
                                              const Stager& st, uint32_t cols, uint32_t acc_stride,
                                              int m, int n0, int n_chunks, bool active,
-                                             uint64_t* tfull,
+                                             bool& cv_left, int& cv_next, bool cv_first,
+                                             const int2* cv_tab, int C,
+                                             const volatile int* progress, uint64_t* tfull,
                                              uint32_t tempty_lead, int& acc, uint32_t& acc_phase,
                                              uint64_t lim, volatile int* abort_flag, int lane) {
   uint32_t sum[NCX];
   IntRow r;
   ColVecs<NCX> V;
-  if constexpr (kEarly) {
+  // (a kernel converting its own operands has its sums only once the MMAs could run)
+  const bool early = kEarly && p.cv_flags == nullptr;
+  if (early) {
     r = int_row(p, m);
     load_col_vecs<NCX>(p, n0, lane, V);
   }
   for (int c = 0; c < n_chunks; ++c) {
+    if (p.cv_flags != nullptr) {
+      // The warp's share of the first band comes first, whenever it waits; then, from
+      // the queue of the later bands, as many jobs as fit before its first
+      // accumulator and one every other chunk after that, none in a unit's last two
+      // chunks: a job taken right after a drain ends before the accumulator after
+      // next is needed, and the unit's outputs are written without conversion
+      // traffic of the warp's own in flight, so the drains (and the MMAs that wait
+      // for them) are not held up.
+      const uint32_t bar = smem_u32(&tfull[acc]);
+      int budget = (cv_first && c == 0) ? 0x7fffffff : ((c & 1) && c < n_chunks - 2 ? 1 : 0);
+      while (__shfl_sync(0xffffffffu, lane == 0 ? (mbar_test_wait(bar, acc_phase) ? 1 : 0) : 0,
+                         0) == 0) {
+        if (cv_static_step<BN, 4>(p, cv_tab, C, cv_next, lane)) continue;
+        if (!cv_left || budget <= 0) break;
+        const int r = cv_step<BN, 4>(p, cv_tab, C, cv_max_band(p, progress), lane);
+        if (r == kCvNone) cv_left = false;
+        if (r != kCvDid) break;
+        --budget;
+      }
+    }
     if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, lim, abort_flag, p.status,
                                             kSiteEpiFull)))
       return false;
@@ -1035,7 +1413,8 @@ __device__ __forceinline__ bool epi_int_unit(const KParams& p, const CUtensorMap
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
-  if constexpr (!kEarly) {
+  if (!early) {
+    if (p.cv_flags != nullptr) cv_acquire_sums<ColVecs<NCX>::kB>(p, m, n0, lane);
     r = int_row(p, m);
     load_col_vecs<NCX>(p, n0, lane, V);
   }
@@ -1078,8 +1457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty_t = full_t + Cfg::kTailStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty_t + Cfg::kTailStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* progress = abort_flag + 1;  // producer: stages issued (read by the prefetch)
+  volatile int* progress = abort_flag + 1;  // producer: stages issued (prefetch, converters)
   int* first_unit = const_cast<int*>(progress) + 1;  // the first unit's Unit fields
+  int2* cv_tab = reinterpret_cast<int2*>(reinterpret_cast<uint8_t*>(bars) + 512);
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
   const int lane = static_cast<int>(lane_id());
@@ -1117,6 +1497,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish_2cta();
   }
   if (warp == 3 && lane == 0) store_first_unit(p, cluster, first_unit);
+  if constexpr (kMode == Mode::GemmInt) {
+    // the conversion jobs' band table: the blocks before each band
+    if (p.cv_flags != nullptr && warp == 2) {
+      const int nb = cv_num_bands(p, num_clusters);
+      for (int b = lane; b <= nb && b < kCvBandTab; b += 32)
+        cv_tab[b] = cv_blocks_before<BN>(p, b, num_clusters);
+    }
+  }
   tc_fence_before();
   // barriers of both CTAs initialised, TMEM allocated in both, first unit known
   cluster_arrive();
@@ -1180,11 +1568,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         cw = qq * p.stride_w - p.pad_w;
       }
       StagePos q{0, 0, 0, 0};
+      // integer GEMM converting its operands: the unit's blocks all done (checked
+      // before the first free slot is waited for, while the ring is still full)
+      bool cv_ready = false;
+      if constexpr (kMode == Mode::GemmInt)
+        if (p.cv_flags != nullptr) cv_ready = cv_unit_ready(p, m_cta, n_cta, lane);
       if (!Cfg::kTailRing || !w.half) {
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, lim, abort_flag,
                                                   p.status, kSiteProducerEmpty)))
             goto producer_done;
+          if constexpr (kMode == Mode::GemmInt) {
+            if (p.cv_flags != nullptr && !cv_ready && kb % p.chunk_kb == 0 &&
+                !cv_wait_chunk(p, m_cta, n_cta, kb / p.chunk_kb, lim, abort_flag, lane))
+              goto producer_done;
+          }
           if (lane == 0) {
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
             load_stage<kMode, ATOMS, Cfg::kAtomBBytes>(
@@ -1220,6 +1618,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t par = ms < sw_stage ? sw_phase : (sw_phase ^ 1u);
             if (!__all_sync(0xffffffffu, mbar_wait(&empty[ms], par, lim, abort_flag, p.status,
                                                     kSiteProducerEmpty)))
+              goto producer_done;
+          }
+          if constexpr (kMode == Mode::GemmInt) {
+            if (p.cv_flags != nullptr && !cv_ready && kb % p.chunk_kb == 0 &&
+                !cv_wait_chunk(p, m_cta, n_cta, kb / p.chunk_kb, lim, abort_flag, lane))
               goto producer_done;
           }
           if (lane == 0) {
@@ -1361,11 +1764,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-    } else if (pair_ok && p.pf_units > 0) {
+    } else if (pair_ok && (p.pf_units > 0 || p.cv_flags != nullptr)) {
     // ------------------------------------------------------------ L2 prefetch (warps 2-3)
+    // or, in an integer GEMM converting its own operands, operand conversion
+      if constexpr (kMode == Mode::GemmInt) {
+        if (p.cv_flags != nullptr) {
+          // until the queue is empty; a job that may not be taken yet is waited
+          // for (bounded: a producer that stopped lets this warp stop too)
+          int next = cv_static_worker(warp);
+          while (cv_static_step<BN, 2>(p, cv_tab, num_clusters, next, lane)) {
+          }
+          uint64_t t_later = 0;
+          for (;;) {
+            const int r = cv_step<BN, 2>(p, cv_tab, num_clusters, cv_max_band(p, progress), lane);
+            if (r == kCvNone || *abort_flag) break;
+            if (r == kCvDid) {
+              t_later = 0;
+            } else {
+              const uint64_t now = globaltimer_ns();
+              if (t_later == 0) t_later = now;
+              if (now - t_later > lim) break;
+              __nanosleep(1000);
+            }
+          }
+        }
+      }
       if constexpr (!mode_is_conv(kMode))
-        prefetch_first_units<BN, Cfg::kKS * 2>(p, cluster, num_clusters, rank,
-                                               (warp - 2) * 32 + lane, progress, abort_flag);
+        if (p.pf_units > 0)
+          prefetch_first_units<BN, Cfg::kKS * 2>(p, cluster, num_clusters, rank,
+                                                 (warp - 2) * 32 + lane, progress, abort_flag);
     }
   } else {
     warpgroup_regs_inc<kRegsHigh>();
@@ -1383,6 +1810,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     st.lane = lane;
     st.M = p.M;
     st.N = p.N;
+    // An integer GEMM converting its own operands: the epilogue warps convert while
+    // they wait for an accumulator (epi_int_unit) until no job is left.
+    bool cv_left = false;
+    int cv_next = cv_static_worker(warp);  // this warp's next first-band job
+    if constexpr (kMode == Mode::GemmInt) cv_left = p.cv_flags != nullptr;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster; u < p.num_units; u += num_clusters) {
@@ -1427,25 +1859,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (two inlined copies of the widest epilogue would not fit the registers:
         // at NC = 128 a half unit keeps the half-0 warps alone)
         bool ok;
+        const bool cv_first = u == cluster;
         if constexpr (NC <= 64) {
-          ok = w.half ? epi_int_unit<NC / 2, true>(
-                            p, tmO0, tmO1, tmO2, st,
-                            lane_base + static_cast<uint32_t>(half * (NC / 2)), Cfg::kAccStride,
-                            m, n0h, n_chunks, true, tfull, tempty_lead, acc, acc_phase, lim,
-                            abort_flag, lane)
-                      : epi_int_unit<NC, true>(
-                            p, tmO0, tmO1, tmO2, st, lane_base + static_cast<uint32_t>(half * NC),
-                            Cfg::kAccStride, m, n0, n_chunks, true, tfull, tempty_lead, acc,
-                            acc_phase, lim, abort_flag, lane);
+          ok = w.half
+                   ? epi_int_unit<BN, NC / 2, true>(
+                         p, tmO0, tmO1, tmO2, st,
+                         lane_base + static_cast<uint32_t>(half * (NC / 2)), Cfg::kAccStride, m,
+                         n0h, n_chunks, true, cv_left, cv_next, cv_first, cv_tab, num_clusters, progress,
+                         tfull, tempty_lead, acc, acc_phase, lim, abort_flag, lane)
+                   : epi_int_unit<BN, NC, true>(
+                         p, tmO0, tmO1, tmO2, st, lane_base + static_cast<uint32_t>(half * NC),
+                         Cfg::kAccStride, m, n0, n_chunks, true, cv_left, cv_next, cv_first, cv_tab,
+                         num_clusters, progress, tfull, tempty_lead, acc, acc_phase, lim,
+                         abort_flag, lane);
         } else {
-          ok = epi_int_unit<NC, false>(p, tmO0, tmO1, tmO2, st,
-                                       lane_base + static_cast<uint32_t>(half * NC),
-                                       Cfg::kAccStride, m, n0, n_chunks, active, tfull,
-                                       tempty_lead, acc, acc_phase, lim, abort_flag, lane);
+          ok = epi_int_unit<BN, NC, false>(
+              p, tmO0, tmO1, tmO2, st, lane_base + static_cast<uint32_t>(half * NC),
+              Cfg::kAccStride, m, n0, n_chunks, active, cv_left, cv_next, cv_first, cv_tab, num_clusters,
+              progress, tfull, tempty_lead, acc, acc_phase, lim, abort_flag, lane);
         }
         if (!ok) goto epi_done;
       }
     }
+    // whatever is left of this warp's first-band share (other CTAs' copies may
+    // wait for it even when this CTA's own units are done)
+    if constexpr (kMode == Mode::GemmInt)
+      if (p.cv_flags != nullptr)
+        while (cv_static_step<BN, 4>(p, cv_tab, num_clusters, cv_next, lane)) {
+        }
   epi_done:
     // every staged store of this warp has completed before the CTA may exit
     if (lane == 0) bulk_wait_group0();

@@ -73,6 +73,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test: true if the phase with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // try_wait with acquire semantics at cluster scope: the phase may have been
 // completed by arrivals (release.cluster) from threads of the peer CTA.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
@@ -190,6 +203,39 @@ __device__ __forceinline__ void bulk_wait_group0() {
 // Makes this thread's ordinary shared-memory writes visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy (TMA) accesses: after ordinary stores that a TMA load elsewhere
+// will read, and before a TMA load of data that ordinary stores wrote.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Load with acquire semantics at GPU scope: later loads of this thread see every
+// write that happened before the release that stored the value read.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Relaxed load at GPU scope (coherent, no ordering by itself): followed by
+// fence_acq_rel_gpu it acquires what the value's release published.
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Atomic add with release semantics at GPU scope: every write of this thread (and
+// every write it has observed) happens before a later acquire that reads the sum.
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -141,7 +141,10 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K,
  *  workspace  device scratch of at least gemm_s8_zp_workspace_size(M, N, K)
  *          bytes, 256-byte aligned, owned by the caller, not shared with a
  *          concurrent call.  It holds the operands shifted to [-128, 127] and
- *          widened to fp16, and their row / column sums.
+ *          widened to fp16, and their row / column sums (whole, or per 1024-k
+ *          chunk with one completion flag per 128 rows and chunk when the
+ *          GEMM kernel converts the operands itself); nothing in it need
+ *          survive between calls.
  *  Rounding: fp32(C32) rounds to nearest even; the product is one fp32
  *  multiply rounded to nearest even; the integer rounding is half-to-even; a
  *  NaN product gives 0.  Results are bit-exact (no tolerance).

@@ -64,6 +64,16 @@ int igc_set_stage_depth(int k);
  *    writing the fp16 operand stages, row / column sums in the same pass): no
  *    pre-pass and no workspace traffic, but about 1.8x the default's time at
  *    8192^3 on GB300, since every output tile converts its own operand panels.
+ *  IGC_INT8_PATH_CONVERT: the default's GEMM kernel with the pre-pass folded
+ *    into it: the CTAs' spare warps convert each 128-row block of the operands,
+ *    1024 k at a time, once, into the workspace (jobs in the order the schedule
+ *    first needs the blocks) while the tensor cores work, and the copies of a
+ *    block wait for its completion flag.  One launch and no separate pass, but
+ *    about 1.04x the default's time at 8192^3 on GB300: the conversion traffic
+ *    shares each SM's path to L2 with the GEMM's own copies, and the first
+ *    round waits for its blocks.  Needs K a multiple of 16 and both operands
+ *    16-byte aligned with row strides that are multiples of 16; other calls
+ *    take the default.
  * Every path gives bit-identical results.  Returns the previous setting, or
  * -1 (and changes nothing) for any other value.  Thread-local: it applies to
  * the calls of the thread that set it and to no other thread's.
@@ -71,6 +81,7 @@ int igc_set_stage_depth(int k);
 #define IGC_INT8_PATH_TCGEN05 0
 #define IGC_INT8_PATH_MMA_SYNC 1
 #define IGC_INT8_PATH_FUSED 2
+#define IGC_INT8_PATH_CONVERT 3
 int igc_set_int8_path(int path);
 
 /*

@@ -37,12 +37,18 @@ def test_status_strings_and_version():
 
 
 def test_workspace_size_arithmetic():
-    # A' (M x Kp fp16) + B' (N x Kp fp16) + row sums + column sums, each 256-aligned
+    # A' (M x Kp fp16) + B' (N x Kp fp16) + row sums + column sums, then the
+    # converting kernel's flags (one per 128-row block and 1024-k chunk, one per
+    # block) and its job counter, each 256-aligned
     def up(v):
         return (v + 255) // 256 * 256
-    for M, N, K in [(1024, 1024, 1024), (8192, 8192, 8192), (3, 5, 7), (1, 1, 1)]:
+    for M, N, K in [(1024, 1024, 1024), (8192, 8192, 8192), (3, 5, 7), (1, 1, 1),
+                    (300, 200, 2064)]:
         Kp = (K + 7) // 8 * 8
-        want = up(M * Kp * 2) + up(N * Kp * 2) + up(4 * M) + up(4 * N)
+        chunks = (K + 1023) // 1024
+        blocks = (M + 127) // 128 + (N + 127) // 128
+        want = (up(M * Kp * 2) + up(N * Kp * 2) + up(4 * M) + up(4 * N) +
+                up(4 * (blocks * chunks + blocks + 1)))
         assert igc.gemm_s8_zp_workspace_size(M, N, K) == want
     assert igc.gemm_s8_zp_workspace_size(-1, 2, 3) == 0
 
@@ -112,9 +118,10 @@ def test_tile_width_setter_roundtrip():
 
 def test_int8_path_setter_roundtrip():
     assert igc.igc_set_int8_path(igc.INT8_PATH_MMA_SYNC) == igc.INT8_PATH_TCGEN05
-    assert igc.igc_set_int8_path(3) == -1            # no such path: unchanged
+    assert igc.igc_set_int8_path(4) == -1            # no such path: unchanged
     assert igc.igc_set_int8_path(igc.INT8_PATH_FUSED) == igc.INT8_PATH_MMA_SYNC
-    assert igc.igc_set_int8_path(igc.INT8_PATH_TCGEN05) == igc.INT8_PATH_FUSED
+    assert igc.igc_set_int8_path(igc.INT8_PATH_CONVERT) == igc.INT8_PATH_FUSED
+    assert igc.igc_set_int8_path(igc.INT8_PATH_TCGEN05) == igc.INT8_PATH_CONVERT
 
 
 def test_stage_depth_setter_roundtrip():
