@@ -409,6 +409,18 @@ def extras_measure(device, peak_tflops: float, hbm_gbs: float, iters: int = 40):
     finally:
         igc.igc_set_int8_path(old_path)
     out["gemm_s8_zp_8192^3_fused_path"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
+    # the same on the converting path (the default kernel's spare warps widen each operand
+    # block once while the tensor cores work; one launch)
+    old_path = igc.igc_set_int8_path(igc.INT8_PATH_CONVERT)
+    try:
+        ms = t_ms(lambda: igc.gemm_s8_zp(Aq, Bq, zA_row=zA, C8=C8w, scale_col=scol,
+                                         workspace=ws))
+    finally:
+        igc.igc_set_int8_path(old_path)
+    out["gemm_s8_zp_8192^3_convert_path"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
+    # the step's int8 GEMM as one call on the default path (pre-pass + GEMM), timed alone
+    ms = t_ms(lambda: igc.gemm_s8_zp(Aq, Bq, zA_row=zA, C8=C8w, scale_col=scol, workspace=ws))
+    out["gemm_s8_zp_8192^3_alone"] = {"ms": ms, "tops": 2 * 8192 ** 3 / ms / 1e9}
     del Aq, Bq, Y, ws, C8w
     # int8 convolution on the layer shape: x uint8 NHWC 256x14x14x256, w int8 512x3x3x256
     x8 = t(synth.uniform_int(43, 6, (256, 14, 14, 256), 0, 255, np.uint8))
