@@ -227,6 +227,8 @@ int run_int_gemm(int64_t M, int64_t N, int64_t K, int a_signed, int b_signed, in
   add_out_map(om, 0, CU_TENSOR_MAP_DATA_TYPE_INT32, C32, ldc32, M, N, 4);
   add_out_map(om, 1, CU_TENSOR_MAP_DATA_TYPE_UINT8, C8, ldc8, M, N, 1);
   add_out_map(om, 2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dq.y, dq.ldy, M, N, 4);
+  if (A_raw != nullptr)
+    return launch_auto_bn<Mode::GemmIntCv>(dev, tmA, ws + l.b_off, Kp, N, Kp * 2, om, p, stream);
   return launch_auto_bn<Mode::GemmInt>(dev, tmA, ws + l.b_off, Kp, N, Kp * 2, om, p, stream);
 }
 

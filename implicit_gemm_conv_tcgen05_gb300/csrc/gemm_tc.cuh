@@ -64,11 +64,22 @@
 
 namespace igc {
 
-enum class Mode : int { GemmF16 = 0, ConvF16 = 1, GemmInt = 2, GemmBF16 = 3, ConvInt = 4 };
+// GemmIntCv: the integer GEMM that converts its own operands (KParams::cv_*), a
+// separate instantiation so that the default integer GEMM carries none of its code.
+enum class Mode : int {
+  GemmF16 = 0,
+  ConvF16 = 1,
+  GemmInt = 2,
+  GemmBF16 = 3,
+  ConvInt = 4,
+  GemmIntCv = 5
+};
 
 // A operand gathered by TMA im2col (a convolution) / integer epilogue
 __host__ __device__ constexpr bool mode_is_conv(Mode m) { return m == Mode::ConvF16 || m == Mode::ConvInt; }
-__host__ __device__ constexpr bool mode_is_int(Mode m) { return m == Mode::GemmInt || m == Mode::ConvInt; }
+__host__ __device__ constexpr bool mode_is_int(Mode m) {
+  return m == Mode::GemmInt || m == Mode::ConvInt || m == Mode::GemmIntCv;
+}
 
 // element type of the floating output
 enum : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
@@ -1034,10 +1045,10 @@ __device__ __forceinline__ void load_col_vec(const void* base, int n0, int N, in
   }
 }
 
-template <int NC>
+template <int NC, bool kCv = false>
 __device__ __forceinline__ void load_col_vecs(const KParams& p, int n0, int lane,
                                               ColVecs<NC>& V) {
-  if (p.cv_flags != nullptr) {
+  if constexpr (kCv) {
 #pragma unroll
     for (int b = 0; b < ColVecs<NC>::kB; ++b) {
       const int n = n0 + 32 * b + lane;
@@ -1079,6 +1090,7 @@ __device__ __forceinline__ IntRow int_row_from(const KParams& p, int m, uint32_t
   return r;
 }
 
+template <bool kCv = false>
 __device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
   const int mm = m < p.M ? m : p.M - 1;  // rows past M are computed (and clipped) like row M-1
   uint32_t rs;
@@ -1094,7 +1106,7 @@ __device__ __forceinline__ IntRow int_row(const KParams& p, int m) {
     for (int r = 0; r < p.conv_R; ++r)
       for (int s = 0; s < p.conv_S; ++s)
         rs += static_cast<uint32_t>(__ldg(base + static_cast<size_t>(r) * p.conv_Wp + s));
-  } else if (p.cv_flags != nullptr) {
+  } else if constexpr (kCv) {
     rs = cv_sum(p, false, mm);
   } else {
     rs = static_cast<uint32_t>(__ldg(p.rsumA + mm));
@@ -1356,7 +1368,7 @@ __device__ __forceinline__ void epi_float_cols(const KParams& p, const CUtensorM
 // fit before the warp's first accumulator, cv_first and chunk 0; one per chunk
 // after that; cv_left turns false once their queue is empty).  Returns false if a
 // wait gave up.
-template <int BN, int NCX, bool kEarly>
+template <int BN, int NCX, bool kEarly, bool kCv>
 __device__ __forceinline__ bool epi_int_unit(const KParams& p, const CUtensorMap& tmO0,
                                              const CUtensorMap& tmO1, const CUtensorMap& tmO2,
                                              const Stager& st, uint32_t cols, uint32_t acc_stride,
@@ -1370,13 +1382,13 @@ __device__ __forceinline__ bool epi_int_unit(const KParams& p, const CUtensorMap
   IntRow r;
   ColVecs<NCX> V;
   // (a kernel converting its own operands has its sums only once the MMAs could run)
-  const bool early = kEarly && p.cv_flags == nullptr;
-  if (early) {
-    r = int_row(p, m);
-    load_col_vecs<NCX>(p, n0, lane, V);
+  constexpr bool early = kEarly && !kCv;
+  if constexpr (early) {
+    r = int_row<kCv>(p, m);
+    load_col_vecs<NCX, kCv>(p, n0, lane, V);
   }
   for (int c = 0; c < n_chunks; ++c) {
-    if (p.cv_flags != nullptr) {
+    if constexpr (kCv) {
       // The warp's share of the first band comes first, whenever it waits; then, from
       // the queue of the later bands, as many jobs as fit before its first
       // accumulator and one every other chunk after that, none in a unit's last two
@@ -1413,10 +1425,10 @@ __device__ __forceinline__ bool epi_int_unit(const KParams& p, const CUtensorMap
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
-  if (!early) {
-    if (p.cv_flags != nullptr) cv_acquire_sums<ColVecs<NCX>::kB>(p, m, n0, lane);
-    r = int_row(p, m);
-    load_col_vecs<NCX>(p, n0, lane, V);
+  if constexpr (!early) {
+    if constexpr (kCv) cv_acquire_sums<ColVecs<NCX>::kB>(p, m, n0, lane);
+    r = int_row<kCv>(p, m);
+    load_col_vecs<NCX, kCv>(p, n0, lane, V);
   }
   if (active) store_row_int_v<NCX>(p, tmO0, tmO1, tmO2, st, m, n0, sum, r, V);
   return true;
@@ -1497,7 +1509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish_2cta();
   }
   if (warp == 3 && lane == 0) store_first_unit(p, cluster, first_unit);
-  if constexpr (kMode == Mode::GemmInt) {
+  if constexpr (kMode == Mode::GemmIntCv) {
     // the conversion jobs' band table: the blocks before each band
     if (p.cv_flags != nullptr && warp == 2) {
       const int nb = cv_num_bands(p, num_clusters);
@@ -1571,14 +1583,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // integer GEMM converting its operands: the unit's blocks all done (checked
       // before the first free slot is waited for, while the ring is still full)
       bool cv_ready = false;
-      if constexpr (kMode == Mode::GemmInt)
+      if constexpr (kMode == Mode::GemmIntCv)
         if (p.cv_flags != nullptr) cv_ready = cv_unit_ready(p, m_cta, n_cta, lane);
       if (!Cfg::kTailRing || !w.half) {
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1u, lim, abort_flag,
                                                   p.status, kSiteProducerEmpty)))
             goto producer_done;
-          if constexpr (kMode == Mode::GemmInt) {
+          if constexpr (kMode == Mode::GemmIntCv) {
             if (p.cv_flags != nullptr && !cv_ready && kb % p.chunk_kb == 0 &&
                 !cv_wait_chunk(p, m_cta, n_cta, kb / p.chunk_kb, lim, abort_flag, lane))
               goto producer_done;
@@ -1620,7 +1632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     kSiteProducerEmpty)))
               goto producer_done;
           }
-          if constexpr (kMode == Mode::GemmInt) {
+          if constexpr (kMode == Mode::GemmIntCv) {
             if (p.cv_flags != nullptr && !cv_ready && kb % p.chunk_kb == 0 &&
                 !cv_wait_chunk(p, m_cta, n_cta, kb / p.chunk_kb, lim, abort_flag, lane))
               goto producer_done;
@@ -1767,7 +1779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (pair_ok && (p.pf_units > 0 || p.cv_flags != nullptr)) {
     // ------------------------------------------------------------ L2 prefetch (warps 2-3)
     // or, in an integer GEMM converting its own operands, operand conversion
-      if constexpr (kMode == Mode::GemmInt) {
+      if constexpr (kMode == Mode::GemmIntCv) {
         if (p.cv_flags != nullptr) {
           // until the queue is empty; a job that may not be taken yet is waited
           // for (bounded: a producer that stopped lets this warp stop too)
@@ -1814,7 +1826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // they wait for an accumulator (epi_int_unit) until no job is left.
     bool cv_left = false;
     int cv_next = cv_static_worker(warp);  // this warp's next first-band job
-    if constexpr (kMode == Mode::GemmInt) cv_left = p.cv_flags != nullptr;
+    if constexpr (kMode == Mode::GemmIntCv) cv_left = p.cv_flags != nullptr;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cluster; u < p.num_units; u += num_clusters) {
@@ -1862,18 +1874,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool cv_first = u == cluster;
         if constexpr (NC <= 64) {
           ok = w.half
-                   ? epi_int_unit<BN, NC / 2, true>(
+                   ? epi_int_unit<BN, NC / 2, true, kMode == Mode::GemmIntCv>(
                          p, tmO0, tmO1, tmO2, st,
                          lane_base + static_cast<uint32_t>(half * (NC / 2)), Cfg::kAccStride, m,
                          n0h, n_chunks, true, cv_left, cv_next, cv_first, cv_tab, num_clusters, progress,
                          tfull, tempty_lead, acc, acc_phase, lim, abort_flag, lane)
-                   : epi_int_unit<BN, NC, true>(
+                   : epi_int_unit<BN, NC, true, kMode == Mode::GemmIntCv>(
                          p, tmO0, tmO1, tmO2, st, lane_base + static_cast<uint32_t>(half * NC),
                          Cfg::kAccStride, m, n0, n_chunks, true, cv_left, cv_next, cv_first, cv_tab,
                          num_clusters, progress, tfull, tempty_lead, acc, acc_phase, lim,
                          abort_flag, lane);
         } else {
-          ok = epi_int_unit<BN, NC, false>(
+          ok = epi_int_unit<BN, NC, false, kMode == Mode::GemmIntCv>(
               p, tmO0, tmO1, tmO2, st, lane_base + static_cast<uint32_t>(half * NC),
               Cfg::kAccStride, m, n0, n_chunks, active, cv_left, cv_next, cv_first, cv_tab, num_clusters,
               progress, tfull, tempty_lead, acc, acc_phase, lim, abort_flag, lane);
@@ -1883,7 +1895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // whatever is left of this warp's first-band share (other CTAs' copies may
     // wait for it even when this CTA's own units are done)
-    if constexpr (kMode == Mode::GemmInt)
+    if constexpr (kMode == Mode::GemmIntCv)
       if (p.cv_flags != nullptr)
         while (cv_static_step<BN, 4>(p, cv_tab, num_clusters, cv_next, lane)) {
         }
