@@ -402,19 +402,21 @@ __device__ __noinline__ void prefetch_first_stages(const KParams& p, const CUten
 }
 
 // ---------------------------------------------------------------------------
-// Integer GEMM converting its own operands (p.cv_flags != nullptr)
+// Integer GEMM converting its own operands (Mode::GemmIntCv, p.cv_flags set)
 //
 // The raw uint8 / int8 operands are shifted and widened to fp16 once, in jobs of
-// 8 rows x one 1024-k chunk that the CTAs' spare warps take from a queue: the
-// epilogue warps while they wait for an accumulator (between two polls of its
-// barrier, one job at a time, so a drain starts at most a job late) and warps 2-3
-// throughout.  A job writes the fp16 values where the copies read them and each
-// row's chunk sum, then adds one to the flag of its 128-row block and chunk; the
-// producer waits for a block's flag before copying that block's chunk.  Jobs come
-// in bands: band b holds the blocks that the schedule's tiles b*C .. (b+1)*C - 1
-// (C CTA pairs: one round of the persistent schedule) use first, chunk after
-// chunk, so the first round's blocks are ready first, and every block is
-// converted once.  No job waits on anything, so the flags always complete.
+// 8 rows x one 1024-k chunk done by the CTAs' spare warps: warps 2-3 throughout,
+// the epilogue warps while they wait for an accumulator (between polls of its
+// barrier, one job at a time; see epi_int_unit).  A job writes the fp16 values
+// where the copies read them and adds each row's chunk sum to the row's sum, then
+// adds one to the flag of its 128-row block and chunk; the producer waits for a
+// block's flag before copying that block's chunk.  Jobs come in bands: band b
+// holds the blocks that the schedule's tiles b*C .. (b+1)*C - 1 (C CTA pairs: one
+// round of the persistent schedule) use first, chunk after chunk, so the first
+// round's blocks are ready first, and every block is converted once.  The first
+// band is shared out statically over the converting warps; the later bands come
+// from one queue, at most one round ahead of the taking CTA's producer.  No job
+// waits on anything, so the flags always complete.
 // ---------------------------------------------------------------------------
 constexpr int kCvRows = 8;                                   // rows of one job
 constexpr int kCvBlockRows = 128;                            // rows under one flag
