@@ -758,7 +758,8 @@ def profile_case(name: str) -> int:
     small: the two small configurations, each called four times (fp16 256^3 with
     fp32 out; int8 1024^3 with C32 + C8).  weak: three weaker extras rows called
     twice each after an L2 flush, in order stride-2 fp16 conv, fp16 512 x 8192 x
-    8192, int8 conv.  Prints the device status word's verdict."""
+    8192, int8 conv.  convert: the step's int8 GEMM (8192^3, C8) on the converting
+    path, called twice after an L2 flush.  Prints the device status word's verdict."""
     import torch
     import implicit_gemm_conv_tcgen05_gb300 as igc
     torch.cuda.set_device(0)
@@ -799,6 +800,21 @@ def profile_case(name: str) -> int:
             igc.gemm_f16(Am, Bk, Cm)
             flush.zero_()
             igc.conv2d_nhwc_s8_zp(x8, w8, 128, y8=y8, scale_k=sk, workspace=wsc)
+    elif name == "convert":
+        w5 = synth.workload(5)
+        Aq, Bq = t(w5["A"]), t(w5["Bt"])
+        zA, sc = t(w5["zA_row"]), t(w5["scale_col"])
+        C8 = torch.empty((8192, 8192), dtype=torch.int8, device="cuda")
+        ws = torch.empty(igc.gemm_s8_zp_workspace_size(8192, 8192, 8192), dtype=torch.uint8,
+                         device="cuda")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        old = igc.igc_set_int8_path(igc.INT8_PATH_CONVERT)
+        try:
+            for _ in range(2):
+                flush.zero_()
+                igc.gemm_s8_zp(Aq, Bq, zA_row=zA, C8=C8, scale_col=sc, workspace=ws)
+        finally:
+            igc.igc_set_int8_path(old)
     else:
         raise ValueError(name)
     torch.cuda.synchronize()
@@ -817,7 +833,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile-case", choices=["small", "weak"], default=None,
+    ap.add_argument("--profile-case", choices=["small", "weak", "convert"], default=None,
                     help="run untimed calls of rows outside the step for an ncu capture")
     args = ap.parse_args(argv)
     if args.profile_case:
