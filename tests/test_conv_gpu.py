@@ -98,6 +98,12 @@ def test_unsupported_stride_reports_status():
     (2, 14, 14, 64, 128, 3, 3, (1, 1), (2, 2)),
     (2, 9, 11, 16, 48, 3, 3, (1, 0), (2, 1)),
     (1, 15, 15, 32, 64, 5, 5, (2, 2), (3, 3)),
+    (3, 28, 28, 128, 96, 3, 3, (1, 1), (2, 2)),      # the strided layer's shape, small batch
+    (2, 12, 12, 256, 64, 1, 1, (0, 0), (2, 2)),      # 1x1 stride 2, two channel blocks
+    (1, 15, 18, 128, 48, 5, 5, (2, 2), (2, 3)),      # stride 3 along W
+    (1, 16, 16, 128, 32, 3, 3, (1, 1), (1, 4)),      # stride 4 along W only
+    (2, 10, 12, 128, 40, 3, 2, (0, 0), (2, 2)),      # no padding, even window
+    (1, 11, 14, 128, 24, 3, 7, (1, 3), (2, 2)),      # wide window with padding 3
 ])
 def test_conv_strided_parity(N, H, W, C, K, R, S, pad, stride):
     x = synth.normal_f16(N * 77 + C, 6, (N, H, W, C))
