@@ -759,7 +759,7 @@ def profile_case(name: str) -> int:
     fp32 out; int8 1024^3 with C32 + C8).  weak: three weaker extras rows called
     twice each after an L2 flush, in order stride-2 fp16 conv, fp16 512 x 8192 x
     8192, int8 conv.  convert: the step's int8 GEMM (8192^3, C8) on the converting
-    path, called twice after an L2 flush.  Prints the device status word's verdict."""
+    path, called twice after an L2 flush.  Prints what the device status word reports."""
     import torch
     import implicit_gemm_conv_tcgen05_gb300 as igc
     torch.cuda.set_device(0)
