@@ -243,3 +243,29 @@ def test_binding_checks_outputs_and_vectors_before_the_device():
         igc.gemm_s8_zp_run(64, 48, 32, 0, 1, ws, C8=C8, scale=1.0)
     with pytest.raises(ValueError, match="Y has shape"):
         igc.gemm_s8_zp_dequant(A, Bt, Y=torch.zeros((64, 47), dtype=torch.float32))
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """With no libigc.so (and none that can be built) every entry point raises:
+    there is no CPU fallback that could return a value instead."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    missing = os.path.join(str(tmp_path), "missing", "libigc.so")
+    code = (
+        "import implicit_gemm_conv_tcgen05_gb300.build as b\n"
+        f"b.build = lambda *a, **k: {missing!r}\n"
+        "import implicit_gemm_conv_tcgen05_gb300 as igc\n"
+        "calls = [lambda: igc.igc_version(), lambda: igc.gemm_s8_zp_workspace_size(8, 8, 8),\n"
+        "         lambda: igc.igc_plan_gemm(igc.PLAN_GEMM_F16, 256, 256, 256, 76)]\n"
+        "for c in calls:\n"
+        "    try:\n"
+        "        c()\n"
+        "    except ImportError:\n"
+        "        continue\n"
+        "    raise SystemExit('a call returned without the library')\n"
+        "print('all raised')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "all raised" in r.stdout
