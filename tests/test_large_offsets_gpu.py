@@ -65,6 +65,27 @@ def test_gemm_f16_operand_beyond_2_gib():
     assert_f16_is_rne_of_f32(host(C16[_on_device(rows)]), c32, "A beyond 2 GiB")
 
 
+def test_gemm_bf16_operand_and_output_beyond_2_gib():
+    M, N, K = 278528, 2048, 4096                      # A: 2.28 GB; bf16 C: 1.14 GB, fp32: 2.28 GB
+    g = _gen(109)
+    A = torch.empty((M, K), dtype=torch.bfloat16, device="cuda").uniform_(-1, 1, generator=g)
+    Bt = torch.empty((N, K), dtype=torch.bfloat16, device="cuda").uniform_(-1, 1, generator=g)
+    C16 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    igc.gemm_bf16(A, Bt, C16, C32)
+    check_device_ok()
+    rows = np.unique(np.concatenate([_crossing(K * 2, M), _crossing(N * 4, M)]))
+    r = _on_device(rows)
+    a_bits = host(A[r].view(torch.int16)).view(np.uint16)
+    b_bits = host(Bt.view(torch.int16)).view(np.uint16)
+    ref, sabs = oracle.gemm_bf16(a_bits, b_bits)
+    c32 = host(C32[r])
+    assert_fp16_bound(c32, ref, sabs, "bf16 beyond 2 GiB, fp32 copy")
+    want = oracle.f32_to_bf16_bits_array(c32)
+    got = host(C16[r].view(torch.int16)).view(np.uint16)
+    assert np.array_equal(got, want), "bf16 outputs are not the RNE rounding of the fp32 copy"
+
+
 @pytest.mark.parametrize("pad", [0, 1])   # row stride N: TMA stores; N + 1: direct stores
 def test_gemm_f16_output_beyond_2_gib(pad):
     M, N, K = 24576, 24576, 64                        # C: 2.42 GB of fp32
