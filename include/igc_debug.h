@@ -73,7 +73,12 @@ int igc_set_stage_depth(int k);
  *    shares each SM's path to L2 with the GEMM's own copies, and the first
  *    round waits for its blocks.  Needs K a multiple of 16 and both operands
  *    16-byte aligned with row strides that are multiples of 16; other calls
- *    take the default.
+ *    take the default.  Its CTAs wait for conversion jobs that other CTAs of
+ *    the same launch do, so it needs all of them resident at once: kernels on
+ *    other streams that hold SMs delay it until they finish, and two such
+ *    calls running at once on different streams can each hold the SMs the
+ *    other's waiting CTAs need, until their bounded waits give up
+ *    (IGC_ERR_DEVICE_TIMEOUT).  Use it from one stream at a time.
  * Every path gives bit-identical results.  Returns the previous setting, or
  * -1 (and changes nothing) for any other value.  Thread-local: it applies to
  * the calls of the thread that set it and to no other thread's.
